@@ -1,0 +1,273 @@
+"""Checks that pin the CPU oracle to things other than itself.
+
+Each check takes the oracle module as an argument so the same checks can be
+run against deliberately broken copies (``test_oracle_mutants.py``): every
+plausible slip in the oracle (a dropped term, a wrong sign, a transposed
+operand, a wrong rounding rule) must make at least one check fail.
+
+What each check stands on:
+  worked_sym / worked_asym  hand-worked values in tests/golden (symmetric: the
+                            aiqz article's worked absmax formula; asymmetric:
+                            the reading written in the fixture)
+  brute_force_codes         nearest grid point by enumerating all 16 codes
+  loss_triple_loop          L written as ||X S^-1 W'hat - X W||^2 with explicit
+                            Python loops (not the difference form, no BLAS)
+  alpha_zero_is_rtn         alpha = 0 gives s = 1: plain RTN group quantisation,
+                            built here by brute force
+  error_bound               |w'hat - w'| <= step * (1/2 + 2^-6)
+  scale_invariance          s -> 2^k s leaves codes and the loss unchanged
+  separability              loss over all columns = sum over a column split
+  act_stats_closed_forms    mean|x| on inputs with a known answer
+  argmin_first / L(a*)<=L(0)
+"""
+from __future__ import annotations
+
+import itertools
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+F32 = np.float32
+
+
+def read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            out[key] = vals
+    return out
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16_round(a):
+    """Round float32 values to bf16 precision (round to nearest even), as float32."""
+    a = np.asarray(a, dtype=F32)
+    u = a.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    u = ((u + 0x7FFF + lsb) >> 16) << 16
+    return u.astype(np.uint32).view(F32)
+
+
+def small_layer(seed, N=16, D_in=16, D_out=16, outliers=(3,), factor=40.0, sigma=0.02):
+    rng = _rng(seed)
+    X = rng.standard_normal((N, D_in)).astype(F32)
+    for j in outliers:
+        X[:, j] *= F32(factor)
+    W = (rng.standard_normal((D_in, D_out)) * sigma).astype(F32)
+    return _bf16_round(X), _bf16_round(W)
+
+
+# ---------------------------------------------------------------------------
+def check_worked_sym(orc):
+    g = read_golden("sym_worked_example.txt")
+    w = np.array([float(v) for v in g["w_s"]], dtype=F32).reshape(-1, 1)
+    codes, step, zero = orc.quantize_groups(w, int(g["group_size"][0]), True)
+    assert float(step[0, 0]) == float(g["delta"][0]), (step, g["delta"])
+    assert [int(c) for c in codes[:, 0]] == [int(v) for v in g["nibble"]], codes[:, 0]
+    assert float(zero[0, 0]) == 8.0
+    deq = orc.dequantize(codes, step, zero, int(g["group_size"][0]))[:, 0]
+    assert np.array_equal(deq, np.array([float(v) for v in g["dequant"]], dtype=F32)), deq
+
+
+def check_worked_asym(orc):
+    g = read_golden("asym_worked_example.txt")
+    w = np.array([float(v) for v in g["w"]], dtype=F32).reshape(-1, 1)
+    codes, step, zero = orc.quantize_groups(w, int(g["group_size"][0]), False)
+    assert float(step[0, 0]) == float(g["step"][0]), step
+    assert float(zero[0, 0]) == float(g["zero"][0]), zero
+    assert [int(c) for c in codes[:, 0]] == [int(v) for v in g["code"]], codes[:, 0]
+    deq = orc.dequantize(codes, step, zero, int(g["group_size"][0]))[:, 0]
+    assert np.array_equal(deq, np.array([float(v) for v in g["dequant"]], dtype=F32)), deq
+
+
+def _nearest_code(x, step, zero, lo, hi):
+    """Code c in [lo, hi] whose dequant (c - zero)*step is nearest x; ties -> even (c - zero)."""
+    best, bestd = None, None
+    for c in range(lo, hi + 1):
+        d = abs(float(x) / float(step) - (c - float(zero)))
+        if bestd is None or d < bestd - 1e-12 or (abs(d - bestd) <= 1e-12 and (c - int(zero)) % 2 == 0):
+            best, bestd = c, d
+    return best
+
+
+def check_brute_force_codes(orc, seed=0):
+    for sym, g in itertools.product((False, True), (8, 16)):
+        rng = _rng(seed + 7 * g + sym)
+        Wp = (rng.standard_normal((32, 12)) * 0.3).astype(F32)
+        Wp[0:g, 0] = np.abs(Wp[0:g, 0])          # a one-signed group
+        Wp[g:2 * g, 1] = -np.abs(Wp[g:2 * g, 1])  # a negative one-signed group
+        codes, step, zero = orc.quantize_groups(Wp, g, sym)
+        lo, hi = (1, 15) if sym else (0, 15)
+        for j in range(Wp.shape[0]):
+            for n in range(Wp.shape[1]):
+                t = j // g
+                st, z = step[t, n], zero[t, n]
+                assert st > 0
+                want = _nearest_code(Wp[j, n], st, z, lo, hi)
+                assert int(codes[j, n]) == want, (sym, g, j, n, codes[j, n], want)
+        # the zero point dequantises to exactly 0
+        assert np.all((zero - zero.astype(np.int64)) == 0)
+        # step is the smallest fp16 value covering the range: range/15 or max/7 rounded
+        Wg = Wp.reshape(-1, g, Wp.shape[1])
+        if sym:
+            want_step = (np.abs(Wg).max(axis=1) / F32(7)).astype(np.float16).astype(F32)
+        else:
+            rngw = np.maximum(Wg.max(axis=1), 0) - np.minimum(Wg.min(axis=1), 0)
+            want_step = (rngw / F32(15)).astype(np.float16).astype(F32)
+        assert np.array_equal(step, want_step)
+
+
+def _scaled_quant_dequant_bruteforce(W, s, g, sym, orc):
+    """S^-1 W'hat built element by element from nearest codes (float64)."""
+    Wp = (W * s[:, None]).astype(F32)
+    _, step, zero = orc.quantize_groups(Wp, g, sym)
+    lo, hi = (1, 15) if sym else (0, 15)
+    out = np.zeros(W.shape, dtype=np.float64)
+    for j in range(W.shape[0]):
+        for n in range(W.shape[1]):
+            t = j // g
+            c = _nearest_code(Wp[j, n], step[t, n], zero[t, n], lo, hi)
+            out[j, n] = (c - float(zero[t, n])) * float(step[t, n]) / float(s[j])
+    return out
+
+
+def check_loss_triple_loop(orc, seed=1):
+    for sym, g in ((False, 8), (True, 16), (False, 16)):
+        X, W = small_layer(seed + g)
+        a = orc.act_stats(X)
+        grid = orc.alpha_grid(5)
+        res = orc.search(X, W, a, grid, group_size=g, symmetric=sym)
+        for k, alpha in enumerate(grid):
+            s = orc.scales(a, alpha)
+            Wh = _scaled_quant_dequant_bruteforce(W, s, g, sym, orc)
+            N, D_in = X.shape
+            D_out = W.shape[1]
+            L = 0.0
+            for r in range(N):
+                for n in range(D_out):
+                    yq = 0.0
+                    y = 0.0
+                    for j in range(D_in):
+                        yq += float(X[r, j]) * Wh[j, n]
+                        y += float(X[r, j]) * float(W[j, n])
+                    L += (yq - y) ** 2
+            got = res["losses"][k]
+            assert abs(got - L) <= 1e-9 * max(L, 1e-30), (sym, g, k, got, L)
+
+
+def check_alpha_zero_is_rtn(orc, seed=2):
+    X, W = small_layer(seed)
+    a = orc.act_stats(X)
+    res = orc.search(X, W, a, orc.alpha_grid(3), group_size=8, symmetric=False)
+    ones = np.ones(W.shape[0], dtype=F32)
+    assert np.array_equal(orc.scales(a, 0.0), ones)
+    Wh = _scaled_quant_dequant_bruteforce(W, ones, 8, False, orc)
+    E = X.astype(np.float64) @ (Wh - W.astype(np.float64))
+    assert abs(res["losses"][0] - float((E * E).sum())) <= 1e-9 * float((E * E).sum())
+
+
+def check_error_bound(orc, seed=3):
+    rng = _rng(seed)
+    for sym in (False, True):
+        W = (rng.standard_normal((256, 64)) * 0.02).astype(F32)
+        s = (rng.uniform(0.5, 30.0, 256)).astype(F32)
+        Wp = (W * s[:, None]).astype(F32)
+        codes, step, zero = orc.quantize_groups(Wp, 128, sym)
+        deq = orc.dequantize(codes, step, zero, 128)
+        err = np.abs(deq - Wp).reshape(2, 128, 64)
+        assert np.all(err <= step[:, None, :] * (0.5 + 2.0 ** -6)), float((err / step[:, None, :]).max())
+
+
+def check_scale_invariance(orc, seed=4):
+    X, W = small_layer(seed, N=24, D_in=32, D_out=8)
+    a = orc.act_stats(X)
+    for sym in (False, True):
+        for alpha in (0.35, 0.8):
+            s = orc.scales(a, alpha)
+            c1, st1, z1 = orc.quantize_groups((W * s[:, None]).astype(F32), 16, sym)
+            s2 = (s * F32(4.0)).astype(F32)
+            c2, st2, z2 = orc.quantize_groups((W * s2[:, None]).astype(F32), 16, sym)
+            assert np.array_equal(c1, c2) and np.array_equal(z1, z2)
+            assert np.array_equal(st2, st1 * F32(4.0))
+            d1 = orc.candidate_delta(W, s, 16, sym)
+            d2 = orc.candidate_delta(W, s2, 16, sym)
+            assert np.array_equal(d1, d2)
+
+
+def check_separability(orc, seed=5):
+    X, W = small_layer(seed, N=20, D_in=32, D_out=24)
+    a = orc.act_stats(X)
+    grid = orc.alpha_grid(6)
+    full = orc.search(X, W, a, grid, group_size=16)
+    left = orc.search(X, W, a, grid, group_size=16, cols=np.arange(0, 10))
+    right = orc.search(X, W, a, grid, group_size=16, cols=np.arange(10, 24))
+    np.testing.assert_allclose(left["losses"] + right["losses"], full["losses"], rtol=1e-12)
+    np.testing.assert_allclose(full["col_losses"][:, 3:5], left["col_losses"][:, 3:5], rtol=1e-12)
+
+
+def check_act_stats_closed_forms(orc):
+    X = np.full((5, 4), -0.75, dtype=F32)
+    assert np.array_equal(orc.act_stats(X), np.full(4, 0.75, dtype=F32))
+    X = np.zeros((8, 3), dtype=F32)
+    X[2] = [4.0, -8.0, 0.5]
+    assert np.array_equal(orc.act_stats(X), np.array([0.5, 1.0, 0.0625], dtype=F32))
+    rng = _rng(6)
+    X = rng.standard_normal((7, 5)).astype(F32)
+    want = []
+    for j in range(5):
+        acc = 0.0
+        for r in range(7):
+            acc += abs(float(X[r, j]))
+        want.append(acc / 7)
+    np.testing.assert_allclose(orc.act_stats(X), np.array(want), rtol=1e-7)
+
+
+def check_argmin_and_improvement(orc, seed=7):
+    X, W = small_layer(seed, N=32, D_in=32, D_out=16, outliers=(1, 9), factor=60.0)
+    a = orc.act_stats(X)
+    res = orc.search(X, W, a, orc.alpha_grid(21), group_size=16)
+    L = res["losses"]
+    assert res["best"] == min(range(len(L)), key=lambda k: (L[k], k))
+    assert L[res["best"]] <= L[0]
+    # with strong outlier channels the scaled search beats plain RTN
+    assert L[0] / L[res["best"]] > 1.0
+    assert np.array_equal(res["s_star"], orc.scales(a, orc.alpha_grid(21)[res["best"]]))
+
+
+def check_pack_layout(orc):
+    W = np.array([[0.875], [-0.4375], [0.0625], [0.1625], [0.225], [-0.875], [0.3125], [0.1875]], dtype=F32)
+    s = np.ones(8, dtype=F32)
+    qw, sc, z = orc.pack(W, s, group_size=8, symmetric=True)
+    # nibbles 15 4 | 8 9 | 10 1 | 10 10 (even row low)
+    assert [int(b) for b in qw[:, 0]] == [0x4F, 0x98, 0x1A, 0xAA], qw[:, 0]
+    assert float(sc[0, 0]) == 0.125 and float(z[0, 0]) == 8.0
+    assert np.array_equal(orc.unpack_codes(qw)[:, 0], np.array([15, 4, 8, 9, 10, 1, 10, 10]))
+
+
+ALL_CHECKS = [
+    check_worked_sym, check_worked_asym, check_brute_force_codes, check_loss_triple_loop,
+    check_alpha_zero_is_rtn, check_error_bound, check_scale_invariance, check_separability,
+    check_act_stats_closed_forms, check_argmin_and_improvement, check_pack_layout,
+]
+
+
+def check_scales_closed_forms(orc):
+    a = np.array([4.0, 0.25, 9.0, 1e-6, 0.0, 2.0], dtype=F32)
+    # alpha = 1 returns the (floored) statistic itself, alpha = 0 returns 1
+    assert np.array_equal(orc.scales(a, 1.0), np.array([4.0, 0.25, 9.0, 1e-4, 1e-4, 2.0], dtype=F32))
+    assert np.array_equal(orc.scales(a, 0.0), np.ones(6, dtype=F32))
+    # alpha = 1/2 is the square root (exact for these values)
+    assert np.array_equal(orc.scales(a[:3], 0.5), np.array([2.0, 0.5, 3.0], dtype=F32))
+    # pow(2, 0.25) rounded to float32
+    assert orc.scales(a[5:], 0.25)[0] == F32(2.0 ** 0.25)
+
+
+ALL_CHECKS.append(check_scales_closed_forms)

@@ -1,0 +1,62 @@
+"""Plant plausible mistakes in copies of the oracle (CPU only) and check that
+the pins catch every one of them."""
+import importlib.util
+import os
+
+import pytest
+
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "awq_oracle.py")
+
+# (name, exact source text, replacement).  Clamping symmetric codes to [-8, 7]
+# instead of [-7, 7] is not listed: with step = max|w|/7 the code -8 is never
+# reached (|w|/step <= 7 * (1 + 2^-11) < 7.5), so that change is equivalent.
+MUTANTS = [
+    ("stat_max_not_mean", "total = np.abs(X64).sum(axis=0)\n    return (total / N)",
+     "total = np.abs(X64).max(axis=0)\n    return (total / 1)"),
+    ("stat_divides_by_N_minus_1", "return (total / N)", "return (total / max(N - 1, 1))"),
+    ("stat_no_abs", "total = np.abs(X64).sum(axis=0)", "total = X64.sum(axis=0)"),
+    ("floor_ignored", "a = np.maximum(np.asarray(mean_abs, dtype=F32), F32(act_floor))",
+     "a = np.asarray(mean_abs, dtype=F32)"),
+    ("sym_divides_by_8", "qmax = 2 ** (bits - 1) - 1", "qmax = 2 ** (bits - 1)"),
+    ("asym_divides_by_16", "qmax = 2 ** bits - 1", "qmax = 2 ** bits"),
+    ("zero_sign_flipped", "zero = np.clip(np.rint(-mn / stepb), 0, qmax)", "zero = np.clip(np.rint(mn / stepb), 0, qmax)"),
+    ("floor_rounding_sym", "q = np.rint(Wg / stepb)", "q = np.floor(Wg / stepb)"),
+    ("half_away_rounding_asym", "q = np.rint(Wg / stepb[:, None, :]) + zero[:, None, :]",
+     "q = np.sign(Wg / stepb[:, None, :]) * np.floor(np.abs(Wg / stepb[:, None, :]) + 0.5) + zero[:, None, :]"),
+    ("step_not_fp16", "h = x.astype(np.float16)", "h = x.astype(np.float32)"),
+    ("range_excludes_zero", "mn = np.minimum(Wg.min(axis=1), F32(0))", "mn = Wg.min(axis=1)"),
+    ("dequant_drops_zero", "return ((c - zero[:, None, :]) * step[:, None, :])", "return ((c) * step[:, None, :])"),
+    ("loss_forgets_inverse_scale", "return What.astype(np.float64) / s.astype(np.float64)[:, None] - W.astype(np.float64)",
+     "return What.astype(np.float64) - W.astype(np.float64)"),
+    ("scales_columns_not_rows", "Wp = W * s[:, None]                                  # W' = diag(s) W, fp32",
+     "Wp = W * s[None, :]"),
+    ("loss_abs_not_square", "return (E * E).sum(axis=0)", "return np.abs(E).sum(axis=0)"),
+    ("argmax_not_argmin", "best = int(np.argmin(losses))", "best = int(np.argmax(losses))"),
+    ("nibbles_swapped", "qweight = (lo | (hi << 4)).astype(np.uint8)", "qweight = (hi | (lo << 4)).astype(np.uint8)"),
+    ("alpha_scaled_twice", "return np.power(a.astype(np.float64), np.float64(alpha)).astype(F32)",
+     "return np.power(a.astype(np.float64), np.float64(2 * alpha)).astype(F32)"),
+]
+
+
+def _load_mutant(name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    src = src.replace(old, new)
+    spec = importlib.util.spec_from_loader(f"awq_oracle_{name}", loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    exec(compile(src, f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new):
+    mod = _load_mutant(name, old, new)
+    caught = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(mod)
+        except Exception:   # an assertion or a crash both count as caught
+            caught.append(check.__name__)
+    assert caught, f"no pin catches mutant {name}"
