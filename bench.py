@@ -1,0 +1,400 @@
+#!/usr/bin/env python
+"""Benchmark of the AWQ calibration hot path on one layer.
+
+One step = the whole path on one synthetic layer whose inputs are resident in
+HBM: act_stats (mean |X|) -> search (21-point alpha grid, candidate losses,
+argmin, s*) -> quantize_pack (int4 codes, fp16 scales / zeros).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload attn_proj]
+
+Prints one JSON line.  `value` is the candidate-GEMM throughput of the whole
+step, 21 * 2 * N * D_in * D_out flops divided by the step time (TFLOP/s),
+summed over ranks (each rank runs its own replica of the layer).  L2 is
+flushed (a 256 MiB write) before every timed step.  Under torchrun each rank
+is one GPU; time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "AWQ alpha-search TFLOP/s & layers/sec (21-pt grid) vs tensor-pipe peak; pack GB/s"
+KERNELS_PER_LAUNCHER = {"act_stats": 2, "scale_table": 1, "group_params": 1, "materialize": 1,
+                        "search_gemm": 1, "reduce_argmin": 3, "pack": 1}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="attn_proj")
+    ap.add_argument("--grid", type=int, default=21)
+    ap.add_argument("--flush-mib", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-cols", type=int, default=0, help="oracle column sample (0 = auto)")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------- helpers
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="awq_clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def workload_bytes(w, G):
+    N, Di, Do, g = w.N, w.D_in, w.D_out, w.group_size
+    flops = 2.0 * N * Di * Do * G
+    stats_bytes = 2.0 * N * Di + 4.0 * Di
+    pack_bytes = 2.0 * Di * Do + 4.0 * Di + Di * Do / 2.0 + 4.0 * Do * Di / g
+    return flops, stats_bytes, pack_bytes
+
+
+# ---------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample_step(w, Xf, Wf, grid, cols):
+    """One bounded step of the CPU oracle: statistic on all rows, search and
+    pack on a column sample.  Returns (seconds, candidate flops of the sample)."""
+    from oracle import awq_oracle as orc
+    t0 = time.perf_counter()
+    a = orc.act_stats(Xf)
+    res = orc.search(Xf, Wf, a, grid, group_size=w.group_size, symmetric=w.symmetric, cols=cols)
+    orc.pack(Wf[:, cols], res["s_star"], group_size=w.group_size, symmetric=w.symmetric)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * w.N * w.D_in * len(cols) * len(grid)
+
+
+def pick_sample_cols(w, requested):
+    if requested:
+        return min(requested, w.D_out)
+    # roughly 10-30 s of single-process numpy/BLAS work on a many-core host
+    budget_flops = 4.0e11
+    n = int(budget_flops / (2.0 * w.N * w.D_in * 21))
+    return max(8, min(w.D_out, n // 8 * 8))
+
+
+def cpu_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        blas = [i.get("num_threads", 0) for i in info if i.get("user_api") == "blas"]
+        if blas:
+            return int(max(blas))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    from post_weight_quantization_column_b300 import synth
+    import numpy as np
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[args.workload]
+    X, W = synth.generate(w)
+    Xf, Wf = synth.bf16_to_f32(X), synth.bf16_to_f32(W)
+    from oracle import awq_oracle as orc
+    grid = orc.alpha_grid(args.grid)
+    ncols = pick_sample_cols(w, args.cpu_sample_cols)
+    # keep the whole run within a few minutes
+    ncols = max(8, ncols // max(1, (args.steps + args.warmup) // 3))
+    cols = synth.sample_columns(w.D_out, ncols, w.seed)
+    for _ in range(args.warmup):
+        oracle_sample_step(w, Xf, Wf, grid, cols)
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample_step(w, Xf, Wf, grid, cols)
+        times.append(dt)
+        flops = fl
+    t = sum(times) / len(times)
+    value = flops / t / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{w.name} N={w.N} D_in={w.D_in} D_out={w.D_out} g={w.group_size} "
+                               f"{'sym' if w.symmetric else 'asym'} G={args.grid}",
+                   "sample": f"{ncols} of {w.D_out} output columns"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"statistic on all rows; search and pack on {ncols} sampled columns",
+                         "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import post_weight_quantization_column_b300 as awq
+    from post_weight_quantization_column_b300 import synth
+
+    if not os.path.exists(awq.LIB_PATH):
+        raise SystemExit("libawq_b300.so is not built: run `python -m post_weight_quantization_column_b300.build`")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = synth.WORKLOADS[args.workload]
+    G = args.grid
+    grid = awq.default_grid(G)
+    X, W = synth.generate(w)
+    Xd, Wd = X.to(dev), W.to(dev)
+    N, Di, Do, g, sym = w.N, w.D_in, w.D_out, w.group_size, w.symmetric
+    T = Di // g
+    a_buf = torch.empty(Di, dtype=torch.float32, device=dev)
+    ws_s = torch.empty(awq.act_stats_workspace_size(N, Di), dtype=torch.uint8, device=dev)
+    ws_q = torch.empty(awq.search_workspace_size(N, Di, Do, G, g, sym), dtype=torch.uint8, device=dev)
+    ws_p = torch.empty(256, dtype=torch.uint8, device=dev)
+    res = awq.SearchResult(torch.empty(G, dtype=torch.float64, device=dev), torch.empty(1, dtype=torch.int32, device=dev),
+                           torch.empty(Di, dtype=torch.float32, device=dev), None, grid, ws_q)
+    pk = (torch.empty(Di // 2, Do, dtype=torch.uint8, device=dev), torch.empty(T, Do, dtype=torch.float16, device=dev),
+          torch.empty(T, Do, dtype=torch.float16, device=dev))
+    flush = torch.empty(args.flush_mib * (1 << 20) // 4, dtype=torch.float32, device=dev)
+
+    def step(Xs, Ws):
+        awq.act_stats(Xs, out=a_buf, ws=ws_s, check=False)
+        awq.search(Xs, Ws, a_buf, grid, g, sym, ws=ws_q, out=res, check=False)
+        awq.quantize_pack(Ws, res.s_star, g, sym, out=pk, ws=ws_p, check=False)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(Xd, Wd)
+    for ws, nm in ((ws_s, "act_stats"), (ws_q, "search"), (ws_p, "pack")):
+        awq.check_workspace(ws, nm)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: inputs resident in HBM
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    awq.profile_enable(True)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record()
+            step(Xd, Wd)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+    barrier(world)
+    kern = awq.profile_collect()
+    awq.profile_enable(False)
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    step_ms_max = max_over_ranks(step_ms, world)
+    clocks = clk.summary()
+
+    flops, stats_bytes, pack_bytes = workload_bytes(w, G)
+    value = world * flops / (step_ms_max * 1e-3) / 1e12
+
+    def per_launch_ms(name):
+        n, tot = kern.get(name, (0, 0.0))
+        return tot / n if n else None
+
+    gemm_ms = per_launch_ms("search_gemm")
+    pack_ms = per_launch_ms("pack")
+    stats_ms = per_launch_ms("act_stats")
+    peaks, peak_src = measured_peaks()
+    achieved = flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
+    roofline = {"kernel": "search_gemm", "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"] if achieved else None,
+                "traffic": None, "peak_source": f"{peak_src} bf16 dense burst",
+                "algorithmic": f"2*N*D_in*D_out*G = {flops:.4g} flop per launch"}
+    tp = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            tj = json.load(f)
+        roofline["traffic"] = tj.get("search_gemm_dram_bytes_per_launch")
+    launches = sum(KERNELS_PER_LAUNCHER.get(k, 1) * n for k, (n, _) in kern.items())
+
+    # ---- end to end through the public API with host buffers
+    Xh = X.pin_memory()
+    Wh = W.pin_memory()
+    Xs = torch.empty_like(Xd)
+    Wsd = torch.empty_like(Wd)
+    outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (*pk, res.losses, res.best_idx, res.s_star)]
+    h2d = Xh.numel() * 2 + Wh.numel() * 2
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record()
+        Xs.copy_(Xh, non_blocking=True)
+        Wsd.copy_(Wh, non_blocking=True)
+        step(Xs, Wsd)
+        for hbuf, dbuf in zip(outs_h, (*pk, res.losses, res.best_idx, res.s_star)):
+            hbuf.copy_(dbuf, non_blocking=True)
+        e2e_ev[i][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    for ws, nm in ((ws_s, "act_stats"), (ws_q, "search"), (ws_p, "pack")):
+        awq.check_workspace(ws, nm)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name} N={N} D_in={Di} D_out={Do} g={g} {'sym' if sym else 'asym'} G={G}",
+                   "l2": f"flushed ({args.flush_mib} MiB write) before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "layers_per_s": world * 1e3 / step_ms_max,
+        "kernels_ms": {k: (tot / n if n else None) for k, (n, tot) in kern.items()},
+        "search_tflops": achieved,
+        "pack_gbs": pack_bytes / (pack_ms * 1e-3) / 1e9 if pack_ms else None,
+        "stats_gbs": stats_bytes / (stats_ms * 1e-3) / 1e9 if stats_ms else None,
+        "hbm_peak_gbs": peaks["hbm_gbs"],
+        "roofline": roofline,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        Xf, Wf = synth.bf16_to_f32(X), synth.bf16_to_f32(W)
+        from oracle import awq_oracle as orc
+        ncols = pick_sample_cols(w, args.cpu_sample_cols)
+        cols = synth.sample_columns(Do, ncols, w.seed)
+        dt, fl = oracle_sample_step(w, Xf, Wf, orc.alpha_grid(G), cols)
+        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                                "sample": f"statistic on all {N} rows; search and pack on {ncols} of {Do} "
+                                          f"columns ({dt:.1f} s)", "cpu": cpu_model()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

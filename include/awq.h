@@ -1,0 +1,169 @@
+/*
+ * awq.h - C ABI of the B300 (sm_103a) AWQ calibration hot path.
+ *
+ * The library computes, for one linear layer Y = X W, the steps of
+ * activation-aware weight quantisation as the pages describe them:
+ *
+ *   1. awq_act_stats      a_j = mean_r |X[r, j]|
+ *   2. awq_search         for every alpha_k of a grid: s_j = max(a_j, floor)^alpha_k,
+ *                         W' = diag(s) W quantised per group of g input rows to
+ *                         4 bits and dequantised, L_k = ||X S^-1 W'hat - X W||^2;
+ *                         then k* = argmin_k L_k and s* = s(alpha_k*)
+ *   3. awq_quantize_pack  Quantize(diag(s) W) as nibble-packed codes plus
+ *                         fp16 per-group scales and zeros
+ *
+ * Sources, by page title and section:
+ *   "AWQ (Activation-aware Weight Quantization)" (compassingai concept page):
+ *       技术原理 - 重要通道识别的统计依据 (statistic), 缩放因子优化的完整流程
+ *       steps 1-6 (grid, scaling, group quantisation, loss, argmin, s*),
+ *       推理时的等效实现 (offline Quantize(diag(s*) W)), 量化数学基础 (absmax).
+ *   aiqz.cc article "awq-activation-aware-quantization", sections 1 and 4
+ *       (E|X_i| importance; Delta = max|w_s|/7, round, clamp, dequant).
+ *   "009. AWQ Integration" (ADR), 关键设计 3 and Consequences (search and
+ *       pack share one quantiser; two 4-bit weights per byte; zeros buffer).
+ *   CSDN AutoAWQ deployment walkthrough, section 2 (quant_config:
+ *       zero_point, q_group_size 128, w_bit 4).
+ *
+ * Conventions shared by every call
+ *   - All matrices are row-major with a contiguous inner dimension.
+ *     X is [N, D_in] bf16 (N calibration rows), W is [D_in, D_out] bf16
+ *     (input channel j = row j; groups run down the rows).
+ *   - Device pointers must be 16-byte aligned; D_in and D_out must be
+ *     multiples of 8.
+ *   - The caller owns every buffer, including the workspace `ws`; the library
+ *     allocates no device memory and keeps no state between calls (other than
+ *     a per-device cache of the architecture check and driver entry points).
+ *   - Every compute call is asynchronous on `stream` (NULL = legacy default
+ *     stream): it validates its arguments on the host, enqueues its kernels
+ *     and returns.  A host-side validation failure returns an error before
+ *     anything is enqueued and before any CUDA call is made.
+ *   - Errors found on the device (a quantisation step that overflows fp16, a
+ *     non-finite input, a bounded wait that expired) are written to a status
+ *     word at the start of `ws`; each call clears that word first.  Read it
+ *     with awq_workspace_status(), which synchronises `stream`.
+ *   - Only sm_103 devices are supported; any other device makes a call
+ *     return AWQ_ERR_UNSUPPORTED_DEVICE.  There is no fallback path.
+ */
+#ifndef AWQ_B300_AWQ_H
+#define AWQ_B300_AWQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define AWQ_API __attribute__((visibility("default")))
+#else
+#define AWQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the same handle type); NULL selects the legacy default stream. */
+typedef struct CUstream_st* awq_stream_t;
+
+typedef enum {
+  AWQ_OK = 0,
+  AWQ_ERR_INVALID_ARG = 1,         /* null pointer, bad cfg field or grid value      */
+  AWQ_ERR_SHAPE = 2,               /* sizes out of range or not divisible             */
+  AWQ_ERR_ALIGNMENT = 3,           /* pointer not 16-byte aligned                     */
+  AWQ_ERR_WORKSPACE = 4,           /* workspace smaller than the size query returned  */
+  AWQ_ERR_UNSUPPORTED_DEVICE = 5,  /* current device is not sm_103                    */
+  AWQ_ERR_CUDA = 6,                /* a CUDA runtime/driver call failed               */
+  AWQ_ERR_RANGE = 7,               /* a quantisation step does not fit in fp16        */
+  AWQ_ERR_NONFINITE = 8,           /* NaN or infinity in an input                     */
+  AWQ_ERR_TIMEOUT = 9              /* a bounded device wait expired (kernel returned) */
+} awq_status;
+
+/* Quantiser configuration (the pages' quant_config: w_bit, q_group_size, zero_point). */
+typedef struct {
+  int32_t bits;        /* must be 4                                                     */
+  int32_t group_size;  /* 64, 128 or 256 input rows per group; must divide D_in         */
+  int32_t symmetric;   /* 0: asymmetric min-max with a zero point; 1: absmax, codes -7..7 */
+  float act_floor;     /* lower clamp of the statistic before the power (1e-4)          */
+} awq_cfg;
+
+/* Human-readable name of a status code (static string, never NULL). */
+AWQ_API const char* awq_status_string(awq_status status);
+
+/* Synchronises `stream` and returns the status word a previous call on the
+ * same workspace left on the device (AWQ_OK if no device error was seen). */
+AWQ_API awq_status awq_workspace_status(const void* ws, awq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Step 1: per-input-channel activation statistic.
+ * "AWQ (Activation-aware Weight Quantization)", 技术原理 - 重要通道识别的统计依据:
+ * activation_scale[j] = mean(|X_calib[:, j]|); aiqz.cc article section 1,
+ * I_i = E[|X_i|].
+ *
+ *   X        device, bf16 [N, D_in], row stride ldx elements (ldx >= D_in, ldx % 8 == 0)
+ *   mean_abs device, fp32 [D_in], written: (1/N) sum_r |X[r, j]|
+ *   ws       device workspace of at least awq_act_stats_workspace_size() bytes
+ * N must be >= 1 (a mean over no rows is undefined: AWQ_ERR_SHAPE); D_in == 0
+ * is a no-op.  Sums are fp32 within a row slice and fp64 across slices, in a
+ * fixed order, so the result is deterministic.  A non-finite X sets
+ * AWQ_ERR_NONFINITE in the workspace status.
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_act_stats_workspace_size(int64_t N, int64_t D_in, size_t* bytes);
+AWQ_API awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t ldx,
+                         float* mean_abs, void* ws, size_t ws_bytes, awq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Steps 2-3: the alpha-grid scale search and its argmin.
+ * "AWQ (Activation-aware Weight Quantization)", 缩放因子优化的完整流程 steps 3-6:
+ * s_j(alpha) = activation_scale[j]^alpha, W' = diag(s) W, W4 per-group
+ * quantisation, L(alpha) = ||X S^-1 W'hat - X W||^2, alpha* = argmin, s*.
+ *
+ *   X          device, bf16 [N, D_in] contiguous
+ *   W          device, bf16 [D_in, D_out] contiguous
+ *   mean_abs   device, fp32 [D_in] (the output of awq_act_stats)
+ *   grid       HOST, fp64 [G] exponents alpha_k in [0, 1] (the pages use k/20, G = 21)
+ *   G          1 <= G <= 64
+ *   losses     device, fp64 [G], written: L_k (plain sum of squares)
+ *   best_idx   device, int32 [1], written: first k with the smallest L_k
+ *   s_star     device, fp32 [D_in], written: s(alpha_best)
+ *   col_losses device, fp64 [G, D_out] or NULL; if given, written with the
+ *              per-output-column share of L_k (L_k = sum_n col_losses[k, n])
+ *   ws         device workspace of at least awq_search_workspace_size() bytes
+ * Scales are s_j = (float)pow((double)max(mean_abs[j], act_floor), alpha_k).
+ * Candidate losses use bf16 tensor-core products with fp32 accumulation and
+ * an fp64 fixed-order reduction; results are deterministic run to run.
+ * N >= 1; D_in a multiple of group_size; D_out a multiple of 8.
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_search_workspace_size(int64_t N, int64_t D_in, int64_t D_out, int32_t G,
+                                     const awq_cfg* cfg, size_t* bytes);
+AWQ_API awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int64_t D_out,
+                      const float* mean_abs, const double* grid, int32_t G, const awq_cfg* cfg,
+                      double* losses, int32_t* best_idx, float* s_star, double* col_losses,
+                      void* ws, size_t ws_bytes, awq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Step 4: offline quantisation and nibble packing of diag(s) W.
+ * "AWQ (Activation-aware Weight Quantization)", 推理时的等效实现:
+ * W_quantized = Quantize(diag(s*) W); "009. AWQ Integration", Consequences:
+ * two 4-bit weights per byte.
+ *
+ *   W        device, bf16 [D_in, D_out] contiguous
+ *   s        device, fp32 [D_in] per-input-channel scale (normally s_star)
+ *   qweight  device, uint8 [D_in/2, D_out]: byte (i, n) = code(2i, n) | code(2i+1, n) << 4
+ *   scales   device, fp16 [D_in/group_size, D_out]: quantisation step per (group, column)
+ *   zeros    device, fp16 [D_in/group_size, D_out]: zero point per (group, column)
+ * Dequantisation is (code - zero) * scale, then / s_j for the original weight.
+ * Asymmetric: step = fp16((max(w',0) - min(w',0)) / 15), zero = clamp(rint(-min/step), 0, 15),
+ *             code = clamp(rint(w'/step) + zero, 0, 15).
+ * Symmetric:  step = fp16(max|w'| / 7), code = clamp(rint(w'/step), -7, 7) + 8, zero = 8.
+ * Divisions are IEEE fp32 round-to-nearest and rint rounds half to even, so
+ * codes, scales and zeros are exact functions of (W, s).  A zero step gives
+ * code 0 (asymmetric, zero 0) or 8 (symmetric).  A step above the fp16 range
+ * sets AWQ_ERR_RANGE; a non-finite W sets AWQ_ERR_NONFINITE.
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_pack_workspace_size(int64_t D_in, int64_t D_out, const awq_cfg* cfg, size_t* bytes);
+AWQ_API awq_status awq_quantize_pack(const void* W, const float* s, int64_t D_in, int64_t D_out,
+                             const awq_cfg* cfg, uint8_t* qweight, void* scales, void* zeros,
+                             void* ws, size_t ws_bytes, awq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AWQ_B300_AWQ_H */

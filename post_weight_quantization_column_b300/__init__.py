@@ -1,0 +1,274 @@
+"""B300 (sm_103a) AWQ calibration hot path: a thin ctypes binding over
+``libawq_b300.so``.
+
+The functions here only marshal torch tensors into the C ABI declared in
+``include/awq.h`` (pointers, sizes, the current CUDA stream); every step of
+the path runs in the library's CUDA kernels.  There is no CPU fallback: if
+the library is missing or the device is not sm_103 the calls raise.
+
+    a = act_stats(X)                                  # mean |X[:, j]|
+    r = search(X, W, a)                               # alpha grid search
+    qweight, scales, zeros = quantize_pack(W, r.s_star)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libawq_b300.so")
+
+AWQ_STATUS = {
+    0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARG", 2: "AWQ_ERR_SHAPE", 3: "AWQ_ERR_ALIGNMENT",
+    4: "AWQ_ERR_WORKSPACE", 5: "AWQ_ERR_UNSUPPORTED_DEVICE", 6: "AWQ_ERR_CUDA",
+    7: "AWQ_ERR_RANGE", 8: "AWQ_ERR_NONFINITE", 9: "AWQ_ERR_TIMEOUT",
+}
+
+
+class AwqError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = AWQ_STATUS.get(code, f"status {code}")
+        super().__init__(f"{where}: {self.name}")
+
+
+class awq_cfg(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("symmetric", ctypes.c_int32), ("act_floor", ctypes.c_float)]
+
+
+class awq_kernel_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
+
+
+_c_i64, _c_i32, _c_sz, _vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
+
+_SIGS = {
+    "awq_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "awq_workspace_status": ([_vp, _vp], ctypes.c_int),
+    "awq_act_stats_workspace_size": ([_c_i64, _c_i64, ctypes.POINTER(_c_sz)], ctypes.c_int),
+    "awq_act_stats": ([_vp, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_sz, _vp], ctypes.c_int),
+    "awq_search_workspace_size": ([_c_i64, _c_i64, _c_i64, _c_i32, ctypes.POINTER(awq_cfg),
+                                   ctypes.POINTER(_c_sz)], ctypes.c_int),
+    "awq_search": ([_vp, _vp, _c_i64, _c_i64, _c_i64, _vp, ctypes.POINTER(ctypes.c_double), _c_i32,
+                    ctypes.POINTER(awq_cfg), _vp, _vp, _vp, _vp, _vp, _c_sz, _vp], ctypes.c_int),
+    "awq_pack_workspace_size": ([_c_i64, _c_i64, ctypes.POINTER(awq_cfg), ctypes.POINTER(_c_sz)], ctypes.c_int),
+    "awq_quantize_pack": ([_vp, _vp, _c_i64, _c_i64, ctypes.POINTER(awq_cfg), _vp, _vp, _vp, _vp, _c_sz, _vp],
+                          ctypes.c_int),
+    "awq_selftest_gemm_bf16": ([_vp, _vp, _c_i32, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_sz, _vp], ctypes.c_int),
+    "awq_profile_enable": ([_c_i32], ctypes.c_int),
+    "awq_profile_collect": ([ctypes.POINTER(awq_kernel_time), _c_i32, ctypes.POINTER(_c_i32)], ctypes.c_int),
+}
+
+_lib = None
+
+
+def lib():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: run `python -m post_weight_quantization_column_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise AwqError(code, where)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t: torch.Tensor, dtype, name):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_cfg(group_size=128, symmetric=False, bits=4, act_floor=1e-4) -> awq_cfg:
+    return awq_cfg(int(bits), int(group_size), 1 if symmetric else 0, float(act_floor))
+
+
+def default_grid(G: int = 21):
+    """alpha_k = k / (G - 1), the pages' {0, 0.05, ..., 1.0} for G = 21."""
+    if G == 1:
+        return [0.0]
+    return [k / (G - 1) for k in range(G)]
+
+
+def workspace_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return the device status word of `ws`."""
+    return lib().awq_workspace_status(_ptr(ws), _stream_handle(stream))
+
+
+def _alloc_ws(nbytes: int, device) -> torch.Tensor:
+    # 256-byte aligned by the caching allocator
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def check_workspace(ws: torch.Tensor, where: str, stream=None):
+    _check(workspace_status(ws, stream), where)
+
+
+# ---------------------------------------------------------------------- step 1
+def act_stats_workspace_size(N: int, D_in: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().awq_act_stats_workspace_size(N, D_in, ctypes.byref(n)), "awq_act_stats_workspace_size")
+    return n.value
+
+
+def act_stats(X: torch.Tensor, out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+              stream=None, check: bool = True) -> torch.Tensor:
+    """mean_r |X[r, j]| for X bf16 [N, D_in] on the GPU -> fp32 [D_in]."""
+    _need(X, torch.bfloat16, "X")
+    N, D = X.shape
+    if out is None:
+        out = torch.empty(D, dtype=torch.float32, device=X.device)
+    if ws is None:
+        ws = _alloc_ws(act_stats_workspace_size(N, D), X.device)
+    st = _stream_handle(stream)
+    _check(lib().awq_act_stats(_ptr(X), N, D, D, _ptr(out), _ptr(ws), ws.numel(), st), "awq_act_stats")
+    if check:
+        check_workspace(ws, "awq_act_stats (device)", stream)
+    return out
+
+
+# ---------------------------------------------------------------------- steps 2-3
+@dataclass
+class SearchResult:
+    losses: torch.Tensor        # fp64 [G]
+    best_idx: torch.Tensor      # int32 [1]
+    s_star: torch.Tensor        # fp32 [D_in]
+    col_losses: Optional[torch.Tensor]  # fp64 [G, D_out] or None
+    grid: list
+    workspace: torch.Tensor
+
+    @property
+    def best(self) -> int:
+        return int(self.best_idx.item())
+
+    @property
+    def alpha_star(self) -> float:
+        return float(self.grid[self.best])
+
+
+def search_workspace_size(N, D_in, D_out, G=21, group_size=128, symmetric=False, act_floor=1e-4) -> int:
+    cfg = make_cfg(group_size, symmetric, 4, act_floor)
+    n = ctypes.c_size_t(0)
+    _check(lib().awq_search_workspace_size(N, D_in, D_out, G, ctypes.byref(cfg), ctypes.byref(n)),
+           "awq_search_workspace_size")
+    return n.value
+
+
+def search(X: torch.Tensor, W: torch.Tensor, mean_abs: torch.Tensor, grid=None, group_size: int = 128,
+           symmetric: bool = False, act_floor: float = 1e-4, col_losses: bool = False,
+           ws: Optional[torch.Tensor] = None, out: Optional[SearchResult] = None, stream=None,
+           check: bool = True) -> SearchResult:
+    """The alpha-grid scale search over X bf16 [N, D_in], W bf16 [D_in, D_out]."""
+    _need(X, torch.bfloat16, "X")
+    _need(W, torch.bfloat16, "W")
+    _need(mean_abs, torch.float32, "mean_abs")
+    N, D_in = X.shape
+    D_in2, D_out = W.shape
+    if D_in2 != D_in or mean_abs.numel() != D_in:
+        raise ValueError("shape mismatch between X, W and mean_abs")
+    grid = list(default_grid() if grid is None else grid)
+    G = len(grid)
+    cfg = make_cfg(group_size, symmetric, 4, act_floor)
+    dev = X.device
+    if ws is None:
+        ws = _alloc_ws(search_workspace_size(N, D_in, D_out, G, group_size, symmetric, act_floor), dev)
+    if out is None:
+        out = SearchResult(torch.empty(G, dtype=torch.float64, device=dev),
+                           torch.empty(1, dtype=torch.int32, device=dev),
+                           torch.empty(D_in, dtype=torch.float32, device=dev),
+                           torch.empty(G, D_out, dtype=torch.float64, device=dev) if col_losses else None,
+                           grid, ws)
+    garr = (ctypes.c_double * G)(*grid)
+    _check(lib().awq_search(_ptr(X), _ptr(W), N, D_in, D_out, _ptr(mean_abs), garr, G, ctypes.byref(cfg),
+                            _ptr(out.losses), _ptr(out.best_idx), _ptr(out.s_star), _ptr(out.col_losses),
+                            _ptr(ws), ws.numel(), _stream_handle(stream)), "awq_search")
+    if check:
+        check_workspace(ws, "awq_search (device)", stream)
+    return out
+
+
+# ---------------------------------------------------------------------- step 4
+def quantize_pack(W: torch.Tensor, s: torch.Tensor, group_size: int = 128, symmetric: bool = False,
+                  out=None, ws: Optional[torch.Tensor] = None, stream=None, check: bool = True):
+    """Quantize(diag(s) W) -> (qweight u8 [D_in/2, D_out], scales fp16 [T, D_out], zeros fp16 [T, D_out])."""
+    _need(W, torch.bfloat16, "W")
+    _need(s, torch.float32, "s")
+    D_in, D_out = W.shape
+    dev = W.device
+    if D_in % group_size:
+        raise ValueError("D_in must be a multiple of group_size")
+    T = D_in // group_size
+    if out is None:
+        out = (torch.empty(D_in // 2, D_out, dtype=torch.uint8, device=dev),
+               torch.empty(T, D_out, dtype=torch.float16, device=dev),
+               torch.empty(T, D_out, dtype=torch.float16, device=dev))
+    qweight, scales, zeros = out
+    cfg = make_cfg(group_size, symmetric)
+    if ws is None:
+        n = ctypes.c_size_t(0)
+        _check(lib().awq_pack_workspace_size(D_in, D_out, ctypes.byref(cfg), ctypes.byref(n)),
+               "awq_pack_workspace_size")
+        ws = _alloc_ws(n.value, dev)
+    _check(lib().awq_quantize_pack(_ptr(W), _ptr(s), D_in, D_out, ctypes.byref(cfg), _ptr(qweight),
+                                   _ptr(scales), _ptr(zeros), _ptr(ws), ws.numel(), _stream_handle(stream)),
+           "awq_quantize_pack")
+    if check:
+        check_workspace(ws, "awq_quantize_pack (device)", stream)
+    return qweight, scales, zeros
+
+
+# ---------------------------------------------------------------------- self-test
+def selftest_gemm(A: torch.Tensor, B: torch.Tensor, b_mn_major: bool = True, stream=None) -> torch.Tensor:
+    """C = A @ B through the library's tensor-core main loop (test helper).
+
+    A bf16 [M, K]; B bf16 [K, N] if b_mn_major else [N, K] (then C = A @ B.T)."""
+    _need(A, torch.bfloat16, "A")
+    _need(B, torch.bfloat16, "B")
+    M, K = A.shape
+    N = B.shape[1] if b_mn_major else B.shape[0]
+    C = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    ws = _alloc_ws(256, A.device)
+    _check(lib().awq_selftest_gemm_bf16(_ptr(A), _ptr(B), 1 if b_mn_major else 0, M, N, K, _ptr(C), _ptr(ws),
+                                        ws.numel(), _stream_handle(stream)), "awq_selftest_gemm_bf16")
+    check_workspace(ws, "awq_selftest_gemm_bf16 (device)", stream)
+    return C
+
+
+# ---------------------------------------------------------------------- profiling aid
+def profile_enable(on: bool = True):
+    """Bracket every library launch with CUDA events on its stream (process-wide)."""
+    _check(lib().awq_profile_enable(1 if on else 0), "awq_profile_enable")
+
+
+def profile_collect() -> dict:
+    """{launcher name: (launches, total_ms)} since the last collect (synchronises the events)."""
+    buf = (awq_kernel_time * 32)()
+    n = ctypes.c_int32(0)
+    _check(lib().awq_profile_collect(buf, 32, ctypes.byref(n)), "awq_profile_collect")
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n.value)}

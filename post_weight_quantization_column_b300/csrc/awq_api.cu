@@ -1,0 +1,386 @@
+// C ABI of the AWQ calibration hot path: argument validation, workspace
+// layout and kernel launch order.  Every function validates on the host
+// first and makes no CUDA call when validation fails.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/awq.h"
+#include "../../include/awq_profile.h"
+#include "../../include/awq_selftest.h"
+#include "internal.h"
+
+using namespace awqdev;
+
+namespace {
+
+constexpr size_t kHeaderBytes = 256;  // status word lives at offset 0
+constexpr int kMaxDevices = 64;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------- device / driver state
+std::mutex g_mu;
+int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+awq_status check_device(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AWQ_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return AWQ_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_arch_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return AWQ_ERR_CUDA;
+    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_arch_ok[dev] != 1) return AWQ_ERR_UNSUPPORTED_DEVICE;
+  if (dev_out) *dev_out = dev;
+  return AWQ_OK;
+}
+
+awq_status get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr)
+      return AWQ_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  *fn = g_encode;
+  return AWQ_OK;
+}
+
+awq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA; }
+
+// ---------------------------------------------------------------- optional event timing
+struct ProfRecord {
+  std::string name;
+  cudaEvent_t start, stop;
+};
+struct Profiler {
+  std::mutex mu;
+  bool enabled = false;
+  std::vector<cudaEvent_t> pool;
+  std::vector<ProfRecord> records;
+  cudaEvent_t take() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+  }
+};
+Profiler g_prof;
+
+// Brackets one launcher call with events on its stream while timing is on.
+class ProfScope {
+ public:
+  ProfScope(const char* name, cudaStream_t s) : name_(name), s_(s) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (!g_prof.enabled) return;
+    start_ = g_prof.take();
+    stop_ = g_prof.take();
+    if (start_ && stop_ && cudaEventRecord(start_, s_) == cudaSuccess) active_ = true;
+  }
+  ~ProfScope() {
+    if (!active_) return;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (cudaEventRecord(stop_, s_) == cudaSuccess) g_prof.records.push_back({name_, start_, stop_});
+  }
+
+ private:
+  const char* name_;
+  cudaStream_t s_;
+  cudaEvent_t start_ = nullptr, stop_ = nullptr;
+  bool active_ = false;
+};
+
+awq_status validate_cfg(const awq_cfg* cfg) {
+  if (!cfg) return AWQ_ERR_INVALID_ARG;
+  if (cfg->bits != 4) return AWQ_ERR_INVALID_ARG;
+  if (cfg->group_size != 64 && cfg->group_size != 128 && cfg->group_size != 256) return AWQ_ERR_INVALID_ARG;
+  if (cfg->symmetric != 0 && cfg->symmetric != 1) return AWQ_ERR_INVALID_ARG;
+  if (!std::isfinite(cfg->act_floor) || cfg->act_floor < 0.f) return AWQ_ERR_INVALID_ARG;
+  return AWQ_OK;
+}
+
+uint32_t* status_word(void* ws) { return static_cast<uint32_t*>(ws); }
+
+// ---------------------------------------------------------------- layouts
+size_t stats_ws_bytes(int64_t N, int64_t D_in) {
+  int splits = 1;
+  int64_t rps = 0;
+  stats_plan(N, D_in, &splits, &rps);
+  return kHeaderBytes + align_up(static_cast<size_t>(splits) * static_cast<size_t>(D_in) * 4, 256);
+}
+
+struct SearchLayout {
+  size_t s_tab, r_tab, qp, partial, col, dW, total;
+  int m_tiles;
+};
+
+SearchLayout search_layout(int64_t N, int64_t D_in, int64_t D_out, int G, int group_size) {
+  SearchLayout L;
+  const size_t g = static_cast<size_t>(G);
+  const size_t din = static_cast<size_t>(D_in), dout = static_cast<size_t>(D_out);
+  L.m_tiles = static_cast<int>((N + kGemmBM - 1) / kGemmBM);
+  size_t off = kHeaderBytes;
+  L.s_tab = off;
+  off = align_up(off + g * din * 4, 256);
+  L.r_tab = off;
+  off = align_up(off + g * din * 4, 256);
+  L.qp = off;
+  off = align_up(off + g * (din / group_size) * dout * sizeof(QParam), 256);
+  L.partial = off;
+  off = align_up(off + g * static_cast<size_t>(L.m_tiles) * dout * 4, 256);
+  L.col = off;
+  off = align_up(off + g * dout * 8, 256);
+  L.dW = off;
+  off = align_up(off + g * din * dout * 2, 256);
+  L.total = off;
+  return L;
+}
+
+awq_status validate_search_shape(int64_t N, int64_t D_in, int64_t D_out, int32_t G, const awq_cfg* cfg) {
+  awq_status st = validate_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (G < 1 || G > kMaxGrid) return AWQ_ERR_SHAPE;
+  if (N < 1 || D_in < 1 || D_out < 1) return AWQ_ERR_SHAPE;
+  if (D_in % cfg->group_size != 0 || D_out % 8 != 0) return AWQ_ERR_SHAPE;
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (N > int64_t(65535) * kGemmBM || D_in > lim / G || D_out > lim) return AWQ_ERR_SHAPE;
+  return AWQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* awq_status_string(awq_status s) {
+  switch (s) {
+    case AWQ_OK: return "AWQ_OK";
+    case AWQ_ERR_INVALID_ARG: return "AWQ_ERR_INVALID_ARG: null pointer or invalid configuration value";
+    case AWQ_ERR_SHAPE: return "AWQ_ERR_SHAPE: sizes out of range or not divisible as required";
+    case AWQ_ERR_ALIGNMENT: return "AWQ_ERR_ALIGNMENT: pointer or leading dimension misaligned";
+    case AWQ_ERR_WORKSPACE: return "AWQ_ERR_WORKSPACE: workspace too small";
+    case AWQ_ERR_UNSUPPORTED_DEVICE: return "AWQ_ERR_UNSUPPORTED_DEVICE: current device is not sm_103";
+    case AWQ_ERR_CUDA: return "AWQ_ERR_CUDA: a CUDA call failed";
+    case AWQ_ERR_RANGE: return "AWQ_ERR_RANGE: quantisation step does not fit in fp16";
+    case AWQ_ERR_NONFINITE: return "AWQ_ERR_NONFINITE: NaN or infinity in an input";
+    case AWQ_ERR_TIMEOUT: return "AWQ_ERR_TIMEOUT: a bounded device wait expired";
+  }
+  return "AWQ_ERR_UNKNOWN";
+}
+
+awq_status awq_workspace_status(const void* ws, awq_stream_t stream) {
+  if (!ws) return AWQ_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  e = cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  return static_cast<awq_status>(word);
+}
+
+// ------------------------------------------------------------------ stats
+awq_status awq_act_stats_workspace_size(int64_t N, int64_t D_in, size_t* bytes) {
+  if (!bytes) return AWQ_ERR_INVALID_ARG;
+  if (N < 1 || D_in < 0) return AWQ_ERR_SHAPE;
+  *bytes = stats_ws_bytes(N, D_in);
+  return AWQ_OK;
+}
+
+awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t ldx, float* mean_abs, void* ws,
+                         size_t ws_bytes, awq_stream_t stream) {
+  if (N < 1 || D_in < 0) return AWQ_ERR_SHAPE;
+  if (D_in == 0) return AWQ_OK;
+  if (!X || !mean_abs || !ws) return AWQ_ERR_INVALID_ARG;
+  if (ldx < D_in || D_in % 8 != 0 || ldx % 8 != 0) return AWQ_ERR_SHAPE;
+  if (!aligned(X, 16) || !aligned(mean_abs, 4) || !aligned(ws, 256)) return AWQ_ERR_ALIGNMENT;
+  if (ws_bytes < stats_ws_bytes(N, D_in)) return AWQ_ERR_WORKSPACE;
+  awq_status st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int splits = 1;
+  int64_t rps = 0;
+  stats_plan(N, D_in, &splits, &rps);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return AWQ_ERR_CUDA;
+  float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
+  ProfScope prof("act_stats", s);
+  return from_cuda(launch_act_stats(X, N, D_in, ldx, mean_abs, partial, splits, rps, status_word(ws), s));
+}
+
+// ------------------------------------------------------------------ search
+awq_status awq_search_workspace_size(int64_t N, int64_t D_in, int64_t D_out, int32_t G, const awq_cfg* cfg,
+                                     size_t* bytes) {
+  if (!bytes) return AWQ_ERR_INVALID_ARG;
+  awq_status st = validate_search_shape(N, D_in, D_out, G, cfg);
+  if (st != AWQ_OK) return st;
+  *bytes = search_layout(N, D_in, D_out, G, cfg->group_size).total;
+  return AWQ_OK;
+}
+
+awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int64_t D_out, const float* mean_abs,
+                      const double* grid, int32_t G, const awq_cfg* cfg, double* losses, int32_t* best_idx,
+                      float* s_star, double* col_losses, void* ws, size_t ws_bytes, awq_stream_t stream) {
+  if (!X || !W || !mean_abs || !grid || !cfg || !losses || !best_idx || !s_star || !ws) return AWQ_ERR_INVALID_ARG;
+  awq_status st = validate_search_shape(N, D_in, D_out, G, cfg);
+  if (st != AWQ_OK) return st;
+  AlphaGrid ag;
+  std::memset(&ag, 0, sizeof(ag));
+  for (int k = 0; k < G; ++k) {
+    if (!std::isfinite(grid[k]) || grid[k] < 0.0 || grid[k] > 1.0) return AWQ_ERR_INVALID_ARG;
+    ag.a[k] = grid[k];
+  }
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(ws, 256) || !aligned(mean_abs, 4) || !aligned(s_star, 4) ||
+      !aligned(losses, 8) || !aligned(best_idx, 4) || (col_losses && !aligned(col_losses, 8)))
+    return AWQ_ERR_ALIGNMENT;
+  const SearchLayout L = search_layout(N, D_in, D_out, G, cfg->group_size);
+  if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
+  st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  st = get_encode(&encode);
+  if (st != AWQ_OK) return st;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint32_t* status = status_word(ws);
+  float* s_tab = reinterpret_cast<float*>(base + L.s_tab);
+  float* r_tab = reinterpret_cast<float*>(base + L.r_tab);
+  QParam* qp = reinterpret_cast<QParam*>(base + L.qp);
+  float* partial = reinterpret_cast<float*>(base + L.partial);
+  double* col = col_losses ? col_losses : reinterpret_cast<double*>(base + L.col);
+  void* dW = base + L.dW;
+
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return AWQ_ERR_CUDA;
+  cudaError_t e;
+  {
+    ProfScope prof("scale_table", s);
+    e = launch_scale_table(mean_abs, D_in, ag, G, cfg->act_floor, s_tab, r_tab, status, s);
+  }
+  if (e == cudaSuccess) {
+    ProfScope prof("group_params", s);
+    e = launch_group_params(W, s_tab, D_in, D_out, G, cfg->group_size, cfg->symmetric, qp, status, s);
+  }
+  if (e == cudaSuccess) {
+    ProfScope prof("materialize", s);
+    e = launch_materialize(W, s_tab, r_tab, qp, D_in, D_out, G, cfg->group_size, cfg->symmetric, dW, s);
+  }
+  if (e == cudaSuccess) {
+    ProfScope prof("search_gemm", s);
+    e = launch_gemm_ssq(encode, X, dW, N, D_out, D_in, G, partial, status, s);
+  }
+  if (e == cudaSuccess) {
+    ProfScope prof("reduce_argmin", s);
+    e = launch_reduce_losses(partial, L.m_tiles, D_out, G, col, losses, best_idx, s_tab, D_in, s_star, status, s);
+  }
+  return from_cuda(e);
+}
+
+// ------------------------------------------------------------------ pack
+awq_status awq_pack_workspace_size(int64_t D_in, int64_t D_out, const awq_cfg* cfg, size_t* bytes) {
+  if (!bytes) return AWQ_ERR_INVALID_ARG;
+  awq_status st = validate_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (D_in < 0 || D_out < 0) return AWQ_ERR_SHAPE;
+  *bytes = kHeaderBytes;
+  return AWQ_OK;
+}
+
+awq_status awq_quantize_pack(const void* W, const float* s, int64_t D_in, int64_t D_out, const awq_cfg* cfg,
+                             uint8_t* qweight, void* scales, void* zeros, void* ws, size_t ws_bytes,
+                             awq_stream_t stream) {
+  awq_status st = validate_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (D_in < 0 || D_out < 0) return AWQ_ERR_SHAPE;
+  if (D_in % cfg->group_size != 0 || D_out % 8 != 0) return AWQ_ERR_SHAPE;
+  if (D_in / cfg->group_size > 65535) return AWQ_ERR_SHAPE;
+  if (D_in == 0 || D_out == 0) return AWQ_OK;
+  if (!W || !s || !qweight || !scales || !zeros || !ws) return AWQ_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(s, 4) || !aligned(qweight, 8) || !aligned(scales, 2) || !aligned(zeros, 2) ||
+      !aligned(ws, 256))
+    return AWQ_ERR_ALIGNMENT;
+  if (ws_bytes < kHeaderBytes) return AWQ_ERR_WORKSPACE;
+  st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return AWQ_ERR_CUDA;
+  ProfScope prof("pack", cs);
+  return from_cuda(launch_pack(W, s, D_in, D_out, cfg->group_size, cfg->symmetric, qweight, scales, zeros,
+                               status_word(ws), cs));
+}
+
+// ------------------------------------------------------------------ self-test GEMM
+awq_status awq_selftest_gemm_bf16(const void* A, const void* B, int32_t b_mn_major, int64_t M, int64_t N, int64_t K,
+                                  float* C, void* ws, size_t ws_bytes, awq_stream_t stream) {
+  if (!A || !B || !C || !ws) return AWQ_ERR_INVALID_ARG;
+  if (M < 1 || N < 8 || K < kGemmBK || K % kGemmBK != 0 || N % 8 != 0 || M > int64_t(65535) * kGemmBM ||
+      K > (int64_t(1) << 30) || N > (int64_t(1) << 30))
+    return AWQ_ERR_SHAPE;
+  if (b_mn_major != 0 && b_mn_major != 1) return AWQ_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 4) || !aligned(ws, 256)) return AWQ_ERR_ALIGNMENT;
+  if (ws_bytes < kHeaderBytes) return AWQ_ERR_WORKSPACE;
+  awq_status st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  st = get_encode(&encode);
+  if (st != AWQ_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return AWQ_ERR_CUDA;
+  return from_cuda(launch_gemm_store(encode, A, B, b_mn_major, M, N, K, C, status_word(ws), cs));
+}
+
+// ------------------------------------------------------------------ profiling
+awq_status awq_profile_enable(int32_t enable) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  g_prof.enabled = enable != 0;
+  return AWQ_OK;
+}
+
+awq_status awq_profile_collect(awq_kernel_time* out, int32_t max_entries, int32_t* n_entries) {
+  if (!n_entries || (max_entries > 0 && !out)) return AWQ_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  std::vector<awq_kernel_time> acc;
+  awq_status st = AWQ_OK;
+  for (const ProfRecord& r : g_prof.records) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+      st = AWQ_ERR_CUDA;
+    size_t i = 0;
+    for (; i < acc.size(); ++i)
+      if (r.name == acc[i].name) break;
+    if (i == acc.size()) {
+      awq_kernel_time t;
+      std::memset(&t, 0, sizeof(t));
+      std::strncpy(t.name, r.name.c_str(), sizeof(t.name) - 1);
+      acc.push_back(t);
+    }
+    acc[i].launches += 1;
+    acc[i].total_ms += ms;
+    g_prof.pool.push_back(r.start);
+    g_prof.pool.push_back(r.stop);
+  }
+  g_prof.records.clear();
+  const int32_t n = static_cast<int32_t>(acc.size()) < max_entries ? static_cast<int32_t>(acc.size()) : max_entries;
+  for (int32_t i = 0; i < n; ++i) out[i] = acc[i];
+  *n_entries = n;
+  return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// Internal launch interface between the C-ABI layer and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "status.h"
+
+namespace awqdev {
+
+// ----------------------------------------------------------------- stats
+constexpr int kStatsThreads = 256;
+constexpr int kStatsRowLanes = 8;      // warps per CTA, each on its own rows
+constexpr int kStatsCols = 256;        // channels per CTA (32 lanes x 8)
+constexpr int kStatsTargetCtas = 148 * 8;
+constexpr int kStatsMaxSplits = 1024;
+
+void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split);
+cudaError_t launch_act_stats(const void* X, int64_t N, int64_t D, int64_t ldx, float* mean_abs, float* partial,
+                             int splits, int64_t rows_per_split, uint32_t* status, cudaStream_t stream);
+
+// ----------------------------------------------------------------- quantiser
+constexpr int kMaxGrid = 64;
+struct AlphaGrid {
+  double a[kMaxGrid];
+};
+
+// Per (candidate, group, column) quantiser parameters used by the search:
+//   inv = 1/step (0 for a zero step), zm = 1.5*2^23 + zero, step.
+struct QParam {
+  float inv, zm, step, pad;
+};
+
+cudaError_t launch_scale_table(const float* mean_abs, int64_t D_in, const AlphaGrid& grid, int G, float act_floor,
+                               float* s_tab, float* r_tab, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in, int64_t D_out, int G,
+                                int group_size, int symmetric, QParam* qp, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r_tab, const QParam* qp,
+                               int64_t D_in, int64_t D_out, int G, int group_size, int symmetric, void* dW,
+                               cudaStream_t stream);
+cudaError_t launch_pack(const void* W, const float* s, int64_t D_in, int64_t D_out, int group_size, int symmetric,
+                        uint8_t* qweight, void* scales, void* zeros, uint32_t* status, cudaStream_t stream);
+
+// ----------------------------------------------------------------- search GEMM
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 256;
+constexpr int kGemmBK = 64;
+
+size_t gemm_smem_bytes();
+// out_partial: [Z][m_tiles][N] per-column sums of squares of X * B_z.
+cudaError_t launch_gemm_ssq(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* A, const void* B, int64_t M,
+                            int64_t N, int64_t K, int Z, float* out_partial, uint32_t* status, cudaStream_t stream);
+// Plain C = A * B in fp32 (self-test of the tensor-core main loop).
+cudaError_t launch_gemm_store(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* A, const void* B, int b_mn_major,
+                              int64_t M, int64_t N, int64_t K, float* C, uint32_t* status, cudaStream_t stream);
+
+// ----------------------------------------------------------------- reductions
+cudaError_t launch_reduce_losses(const float* partial, int m_tiles, int64_t D_out, int G, double* col_losses,
+                                 double* losses, int32_t* best_idx, const float* s_tab, int64_t D_in, float* s_star,
+                                 uint32_t* status, cudaStream_t stream);
+
+}  // namespace awqdev

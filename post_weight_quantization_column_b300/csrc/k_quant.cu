@@ -1,0 +1,432 @@
+// Scale table, per-group quantiser parameters, candidate materialisation and
+// the bit-exact int4 pack.
+//
+// Quantiser ("AWQ (Activation-aware Weight Quantization)", 技术原理 -
+// 量化数学基础; aiqz.cc article "awq-activation-aware-quantization", section 4;
+// asymmetric zero-point form of the CSDN AutoAWQ walkthrough's quant_config):
+//   asymmetric: step = fp16((max(w',0) - min(w',0)) / 15), zero = clamp(rint(-min/step), 0, 15),
+//               code = clamp(rint(w'/step) + zero, 0, 15)
+//   symmetric:  step = fp16(max|w'| / 7), code = clamp(rint(w'/step), -7, 7) (+8 when stored)
+//   dequant (code - zero) * step; a zero step gives dequant 0.
+// The pack reproduces the IEEE fp32 round-to-nearest quotient w'/step exactly;
+// the search uses a reciprocal multiply (its loss tolerance allows it).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace awqdev {
+
+// 1.5 * 2^23: adding it to |x| < 2^22 rounds x to an integer (ties to even)
+// held in the low mantissa bits.
+constexpr float kMagic = 12582912.0f;
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+__device__ __forceinline__ bool bf16x2_nonfinite(uint32_t u) {
+  return ((u & 0x7F80u) == 0x7F80u) || ((u & 0x7F800000u) == 0x7F800000u);
+}
+
+// ------------------------------------------------------------------ scales
+// s_kj = fp32(pow(fp64(max(a_j, floor)), alpha_k)), r_kj = 1/s_kj (IEEE).
+// "AWQ (Activation-aware Weight Quantization)", 缩放因子优化的完整流程 step 3.
+__global__ void scale_table_kernel(const float* __restrict__ mean_abs, int64_t D, AlphaGrid grid, float act_floor,
+                                   float* __restrict__ s_tab, float* __restrict__ r_tab, uint32_t* status) {
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int k = blockIdx.y;
+  if (j >= D) return;
+  const float a = mean_abs[j];
+  if (!isfinite(a) && k == 0) set_error(status, AWQ_DEV_NONFINITE);
+  const float af = fmaxf(a, act_floor);
+  const float s = static_cast<float>(pow(static_cast<double>(af), grid.a[k]));
+  s_tab[static_cast<int64_t>(k) * D + j] = s;
+  r_tab[static_cast<int64_t>(k) * D + j] = __fdiv_rn(1.0f, s);
+}
+
+cudaError_t launch_scale_table(const float* mean_abs, int64_t D_in, const AlphaGrid& grid, int G, float act_floor,
+                               float* s_tab, float* r_tab, uint32_t* status, cudaStream_t stream) {
+  const dim3 g(static_cast<unsigned>((D_in + 255) / 256), static_cast<unsigned>(G));
+  scale_table_kernel<<<g, 256, 0, stream>>>(mean_abs, D_in, grid, act_floor, s_tab, r_tab, status);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ group parameters
+// Exact step / zero of one (group, column) from the range of its scaled weights.
+__device__ __forceinline__ QParam make_qparam(float lo, float hi, int symmetric, uint32_t* status) {
+  QParam q;
+  q.pad = 0.f;
+  const float raw = symmetric ? __fdiv_rn(hi, 7.0f) : __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  float sc = __half2float(__float2half_rn(raw));
+  if (isinf(sc)) {
+    set_error(status, AWQ_DEV_RANGE);
+    sc = 0.f;
+  }
+  if (sc == 0.f) {
+    q.inv = 0.f;
+    q.zm = kMagic;
+    q.step = 0.f;
+    return q;
+  }
+  float z = 0.f;
+  if (!symmetric) z = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.f), 15.f);
+  q.inv = __frcp_rn(sc);
+  q.zm = kMagic + z;
+  q.step = sc;
+  return q;
+}
+
+// One CTA: one group of GS rows x 256 columns, all G candidates.  The W tile
+// and the group's slice of the scale table sit in shared memory; each thread
+// owns two adjacent columns and scans the group once per candidate.
+template <int GS>
+__global__ void __launch_bounds__(128) group_params_kernel(const __nv_bfloat16* __restrict__ W,
+                                                         const float* __restrict__ s_tab, int64_t D_in,
+                                                         int64_t D_out, int G, int symmetric,
+                                                         QParam* __restrict__ qp, uint32_t* status) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t* wsh = reinterpret_cast<uint32_t*>(smem);             // [GS][128] bf16 pairs
+  float* ssh = reinterpret_cast<float*>(smem + GS * 128 * 4);    // [G][GS]
+  const int t = threadIdx.x;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 256;
+  const int64_t grp = blockIdx.y;
+  const int64_t j0 = grp * GS;
+  bool bad = false;
+  for (int idx = t; idx < GS * 32; idx += 128) {
+    const int r = idx >> 5;
+    const int c8 = idx & 31;
+    const int64_t col = n0 + c8 * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (col < D_out) v = *reinterpret_cast<const uint4*>(W + (j0 + r) * D_out + col);
+    bad |= bf16x2_nonfinite(v.x) | bf16x2_nonfinite(v.y) | bf16x2_nonfinite(v.z) | bf16x2_nonfinite(v.w);
+    *reinterpret_cast<uint4*>(&wsh[r * 128 + c8 * 4]) = v;
+  }
+  for (int idx = t; idx < G * GS; idx += 128) {
+    const int k = idx / GS;
+    const int r = idx - k * GS;
+    ssh[idx] = s_tab[static_cast<int64_t>(k) * D_in + j0 + r];
+  }
+  if (bad) set_error(status, AWQ_DEV_NONFINITE);
+  __syncthreads();
+  const int64_t n = n0 + 2 * t;
+  const int64_t T = D_in / GS;
+  for (int k = 0; k < G; ++k) {
+    const float* sk = ssh + k * GS;
+    float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;
+    if (symmetric) {
+#pragma unroll 8
+      for (int r = 0; r < GS; ++r) {
+        const uint32_t u = wsh[r * 128 + t];
+        const float s = sk[r];
+        hi0 = fmaxf(hi0, fabsf(__fmul_rn(bf16lo(u), s)));
+        hi1 = fmaxf(hi1, fabsf(__fmul_rn(bf16hi(u), s)));
+      }
+    } else {
+#pragma unroll 8
+      for (int r = 0; r < GS; ++r) {
+        const uint32_t u = wsh[r * 128 + t];
+        const float s = sk[r];
+        const float p0 = __fmul_rn(bf16lo(u), s);
+        const float p1 = __fmul_rn(bf16hi(u), s);
+        lo0 = fminf(lo0, p0);
+        hi0 = fmaxf(hi0, p0);
+        lo1 = fminf(lo1, p1);
+        hi1 = fmaxf(hi1, p1);
+      }
+    }
+    if (n < D_out) {
+      QParam* dst = qp + (static_cast<int64_t>(k) * T + grp) * D_out + n;
+      dst[0] = make_qparam(lo0, hi0, symmetric, status);
+      dst[1] = make_qparam(lo1, hi1, symmetric, status);
+    }
+  }
+}
+
+static size_t group_params_smem(int GS, int G) { return static_cast<size_t>(GS) * 512 + static_cast<size_t>(G) * GS * 4; }
+
+cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in, int64_t D_out, int G,
+                                int group_size, int symmetric, QParam* qp, uint32_t* status, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>((D_out + 255) / 256), static_cast<unsigned>(D_in / group_size));
+  const size_t smem = group_params_smem(group_size, G);
+  const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
+  cudaError_t e;
+  switch (group_size) {
+    case 64:
+      e = cudaFuncSetAttribute(group_params_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      group_params_kernel<64><<<grid, 128, smem, stream>>>(Wb, s_tab, D_in, D_out, G, symmetric, qp, status);
+      break;
+    case 128:
+      e = cudaFuncSetAttribute(group_params_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      group_params_kernel<128><<<grid, 128, smem, stream>>>(Wb, s_tab, D_in, D_out, G, symmetric, qp, status);
+      break;
+    case 256:
+      e = cudaFuncSetAttribute(group_params_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      group_params_kernel<256><<<grid, 128, smem, stream>>>(Wb, s_tab, D_in, D_out, G, symmetric, qp, status);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ candidate materialisation
+// dW_k[j, n] = bf16( (code - zero) * step / s_kj - w_jn ): the difference form
+// S^-1 W'hat - W of one candidate, so that X * dW_k is the output error of
+// "AWQ (Activation-aware Weight Quantization)", 缩放因子优化的完整流程 step 4c.
+__device__ __forceinline__ float dq_delta(float w, float s, float r, const QParam& q, float lo, float hi) {
+  const float wp = w * s;
+  float t = fmaf(wp, q.inv, q.zm);
+  t = fminf(fmaxf(t, lo), hi);
+  const float d = (t - q.zm) * q.step;
+  return fmaf(d, r, -w);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(256) materialize_kernel(const __nv_bfloat16* __restrict__ W,
+                                                        const float* __restrict__ s_tab,
+                                                        const float* __restrict__ r_tab,
+                                                        const QParam* __restrict__ qp, int64_t D_in, int64_t D_out,
+                                                        int group_size, float lo, float hi,
+                                                        __nv_bfloat16* __restrict__ dW) {
+  const int lane = threadIdx.x & 31;
+  const int rl = threadIdx.x >> 5;
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * 256 + lane * 8;
+  if (n >= D_out) return;
+  const int k = blockIdx.z;
+  const int64_t jb = static_cast<int64_t>(blockIdx.y) * 64;
+  const int64_t T = D_in / group_size;
+  const int64_t grp = jb / group_size;
+  const QParam* q = qp + (static_cast<int64_t>(k) * T + grp) * D_out + n;
+  QParam qv[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) qv[c] = q[c];
+#pragma unroll 2
+  for (int i = 0; i < 8; ++i) {
+    const int64_t j = jb + rl + 8 * i;
+    const float s = s_tab[static_cast<int64_t>(k) * D_in + j];
+    const float r = r_tab[static_cast<int64_t>(k) * D_in + j];
+    const uint4 wv = *reinterpret_cast<const uint4*>(W + j * D_out + n);
+    const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float d0 = dq_delta(bf16lo(wu[c]), s, r, qv[2 * c], lo, hi);
+      const float d1 = dq_delta(bf16hi(wu[c]), s, r, qv[2 * c + 1], lo, hi);
+      o[c] = pack_bf16x2(d0, d1);
+    }
+    *reinterpret_cast<uint4*>(dW + (static_cast<int64_t>(k) * D_in + j) * D_out + n) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r_tab, const QParam* qp,
+                               int64_t D_in, int64_t D_out, int G, int group_size, int symmetric, void* dW,
+                               cudaStream_t stream) {
+  const float lo = symmetric ? kMagic - 7.f : kMagic;
+  const float hi = symmetric ? kMagic + 7.f : kMagic + 15.f;
+  const dim3 grid(static_cast<unsigned>((D_out + 255) / 256), static_cast<unsigned>(D_in / 64),
+                  static_cast<unsigned>(G));
+  materialize_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(W), s_tab, r_tab, qp, D_in, D_out,
+                                               group_size, lo, hi, static_cast<__nv_bfloat16*>(dW));
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ pack
+// "AWQ (Activation-aware Weight Quantization)", 推理时的等效实现:
+// W_quantized = Quantize(diag(s*) W); "009. AWQ Integration", Consequences:
+// two 4-bit codes per byte (even input row in the low nibble).
+//
+// One CTA: one group (GS rows) x 256 columns.  Lane l of warp w owns columns
+// [8l, 8l+8) and rows [w*RPT, (w+1)*RPT), RPT = GS/8, held in registers as
+// bf16 pairs.  Pass 1 finds the per-column range (fixed-order combine of the
+// 8 warps in shared memory) and the exact step / zero; pass 2 emits codes.
+//
+// Codes equal clamp(rint(fp32(w'/step)) + zero): the quotient is first
+// formed as w' * (1/step); where that lands within 8e-6 of a half-integer
+// (where the two could round differently), the thread redoes its rows with
+// the IEEE division.  |w'/step| <= 45 in every case, where the product is
+// within 6e-6 of the IEEE quotient, so elsewhere both round alike.
+constexpr float kTieGuard = 0.5f - 8.0e-6f;
+
+template <int RPT>
+__global__ void __launch_bounds__(256) pack_kernel(const __nv_bfloat16* __restrict__ W, const float* __restrict__ s,
+                                                 int64_t D_in, int64_t D_out, int symmetric,
+                                                 uint8_t* __restrict__ qweight, __half* __restrict__ scales,
+                                                 __half* __restrict__ zeros, uint32_t* status) {
+  constexpr int GS = RPT * 8;
+  __shared__ float red_lo[8][256];
+  __shared__ float red_hi[8][256];
+  __shared__ float4 prm[256];   // {step, 1/step, zoff, zero}
+  const int lane = threadIdx.x & 31;
+  const int wp_ = threadIdx.x >> 5;
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * 256 + lane * 8;
+  const int64_t grp = blockIdx.y;
+  const int64_t j0 = grp * GS + wp_ * RPT;
+  const bool active = n < D_out;
+
+  uint4 w[RPT];
+  float sj[RPT];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    sj[i] = s[j0 + i];
+    w[i] = active ? *reinterpret_cast<const uint4*>(W + (j0 + i) * D_out + n) : make_uint4(0u, 0u, 0u, 0u);
+    bad |= bf16x2_nonfinite(w[i].x) | bf16x2_nonfinite(w[i].y) | bf16x2_nonfinite(w[i].z) |
+           bf16x2_nonfinite(w[i].w);
+  }
+  if (bad) set_error(status, AWQ_DEV_NONFINITE);
+
+  // pass 1: per-column range of w' = w * s over this thread's rows
+  float lo[8], hi[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) lo[c] = hi[c] = 0.f;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const uint32_t wu[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float p0 = __fmul_rn(bf16lo(wu[c]), sj[i]);
+      const float p1 = __fmul_rn(bf16hi(wu[c]), sj[i]);
+      if (symmetric) {
+        hi[2 * c] = fmaxf(hi[2 * c], fabsf(p0));
+        hi[2 * c + 1] = fmaxf(hi[2 * c + 1], fabsf(p1));
+      } else {
+        lo[2 * c] = fminf(lo[2 * c], p0);
+        hi[2 * c] = fmaxf(hi[2 * c], p0);
+        lo[2 * c + 1] = fminf(lo[2 * c + 1], p1);
+        hi[2 * c + 1] = fmaxf(hi[2 * c + 1], p1);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    red_lo[wp_][lane * 8 + c] = lo[c];
+    red_hi[wp_][lane * 8 + c] = hi[c];
+  }
+  __syncthreads();
+  {
+    const int col = threadIdx.x;
+    float l = 0.f, h = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      l = fminf(l, red_lo[k][col]);
+      h = fmaxf(h, red_hi[k][col]);
+    }
+    const float raw = symmetric ? __fdiv_rn(h, 7.0f) : __fdiv_rn(__fsub_rn(h, l), 15.0f);
+    float sc = __half2float(__float2half_rn(raw));
+    if (isinf(sc)) {
+      set_error(status, AWQ_DEV_RANGE);
+      sc = 0.f;
+    }
+    float z = 0.f;
+    if (!symmetric && sc != 0.f) z = fminf(fmaxf(rintf(__fdiv_rn(-l, sc)), 0.f), 15.f);
+    const float zoff = symmetric ? 8.f : z;
+    prm[col] = make_float4(sc, sc != 0.f ? __frcp_rn(sc) : 0.f, zoff, symmetric ? 8.f : z);
+    const int64_t ncol = static_cast<int64_t>(blockIdx.x) * 256 + col;
+    if (ncol < D_out) {
+      scales[grp * D_out + ncol] = __float2half_rn(sc);
+      zeros[grp * D_out + ncol] = __float2half_rn(symmetric ? 8.f : z);
+    }
+  }
+  __syncthreads();
+  if (!active) return;
+
+  float step[8], inv[8], zmz[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float4 p = prm[lane * 8 + c];
+    step[c] = p.x;
+    inv[c] = p.y;
+    zmz[c] = kMagic + p.z;
+  }
+  const float clo = symmetric ? kMagic + 1.f : kMagic;
+  const float chi = kMagic + 15.f;
+
+  // pass 2 (fast): codes through the reciprocal, with a near-tie flag
+  uint32_t out[RPT / 2][2];
+  bool tie = false;
+#pragma unroll
+  for (int i = 0; i < RPT; i += 2) {
+    const uint32_t we[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+    const uint32_t wo[4] = {w[i + 1].x, w[i + 1].y, w[i + 1].z, w[i + 1].w};
+    uint32_t bytes[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float xe = (c & 1) ? bf16hi(we[c >> 1]) : bf16lo(we[c >> 1]);
+      const float xo = (c & 1) ? bf16hi(wo[c >> 1]) : bf16lo(wo[c >> 1]);
+      const float ye = __fmul_rn(__fmul_rn(xe, sj[i]), inv[c]);
+      const float yo = __fmul_rn(__fmul_rn(xo, sj[i + 1]), inv[c]);
+      float ce = __fadd_rn(ye, zmz[c]);
+      float co = __fadd_rn(yo, zmz[c]);
+      tie |= fabsf(__fsub_rn(ye, __fsub_rn(ce, zmz[c]))) > kTieGuard;
+      tie |= fabsf(__fsub_rn(yo, __fsub_rn(co, zmz[c]))) > kTieGuard;
+      ce = fminf(fmaxf(ce, clo), chi);
+      co = fminf(fmaxf(co, clo), chi);
+      bytes[c] = (__float_as_uint(ce) & 0xFu) | ((__float_as_uint(co) & 0xFu) << 4);
+    }
+    out[i / 2][0] = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+    out[i / 2][1] = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+  }
+  if (tie) {
+    // slow path: IEEE quotient for every element of this thread
+#pragma unroll
+    for (int i = 0; i < RPT; i += 2) {
+      const uint32_t we[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+      const uint32_t wo[4] = {w[i + 1].x, w[i + 1].y, w[i + 1].z, w[i + 1].w};
+      uint32_t bytes[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float xe = (c & 1) ? bf16hi(we[c >> 1]) : bf16lo(we[c >> 1]);
+        const float xo = (c & 1) ? bf16hi(wo[c >> 1]) : bf16lo(wo[c >> 1]);
+        // clamp(rint(IEEE w'/step) + zoff, clo, 15); a zero step keeps code zoff
+        uint32_t ke = static_cast<uint32_t>(zmz[c] - kMagic), ko = ke;
+        if (step[c] != 0.f) {
+          const float zo = zmz[c] - kMagic;
+          const float ql = clo - kMagic;
+          const float qe = rintf(__fdiv_rn(__fmul_rn(xe, sj[i]), step[c])) + zo;
+          const float qo = rintf(__fdiv_rn(__fmul_rn(xo, sj[i + 1]), step[c])) + zo;
+          ke = static_cast<uint32_t>(fminf(fmaxf(qe, ql), 15.f));
+          ko = static_cast<uint32_t>(fminf(fmaxf(qo, ql), 15.f));
+        }
+        bytes[c] = ke | (ko << 4);
+      }
+      out[i / 2][0] = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+      out[i / 2][1] = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < RPT; i += 2) {
+    const int64_t row = (j0 + i) / 2;
+    *reinterpret_cast<uint2*>(qweight + row * D_out + n) = make_uint2(out[i / 2][0], out[i / 2][1]);
+  }
+}
+
+cudaError_t launch_pack(const void* W, const float* s, int64_t D_in, int64_t D_out, int group_size, int symmetric,
+                        uint8_t* qweight, void* scales, void* zeros, uint32_t* status, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>((D_out + 255) / 256), static_cast<unsigned>(D_in / group_size));
+  const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
+  __half* sc = static_cast<__half*>(scales);
+  __half* zr = static_cast<__half*>(zeros);
+  switch (group_size) {
+    case 64:
+      pack_kernel<8><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
+      break;
+    case 128:
+      pack_kernel<16><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
+      break;
+    case 256:
+      pack_kernel<32><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace awqdev
