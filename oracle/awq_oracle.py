@@ -145,7 +145,7 @@ def quantize_groups(Wp: np.ndarray, group_size: int, symmetric: bool, bits: int 
         ok = step > 0
         stepb = np.where(ok, step, F32(1))
         zero = np.clip(np.rint(-mn / stepb), 0, qmax).astype(F32)
-        zero = np.where(ok, zero, F32(0))
+        zero = np.where(ok, zero, F32(0)) + F32(0)   # an integer code: -0 becomes +0
         q = np.rint(Wg / stepb[:, None, :]) + zero[:, None, :]
         q = np.clip(q, 0, qmax)
         q = np.where(ok[:, None, :], q, F32(0))

@@ -69,7 +69,8 @@ __device__ __forceinline__ QParam make_qparam(float lo, float hi, int symmetric,
     return q;
   }
   float z = 0.f;
-  if (!symmetric) z = fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.f), 15.f);
+  // an integer code in [0, 15]; the int round trip also turns -0 into +0
+  if (!symmetric) z = static_cast<float>(static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(-lo, sc)), 0.f), 15.f)));
   q.inv = __frcp_rn(sc);
   q.zm = kMagic + z;
   q.step = sc;
@@ -325,7 +326,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const __nv_bfloat16* __restri
       sc = 0.f;
     }
     float z = 0.f;
-    if (!symmetric && sc != 0.f) z = fminf(fmaxf(rintf(__fdiv_rn(-l, sc)), 0.f), 15.f);
+    if (!symmetric && sc != 0.f)
+      z = static_cast<float>(static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(-l, sc)), 0.f), 15.f)));
     const float zoff = symmetric ? 8.f : z;
     prm[col] = make_float4(sc, sc != 0.f ? __frcp_rn(sc) : 0.f, zoff, symmetric ? 8.f : z);
     const int64_t ncol = static_cast<int64_t>(blockIdx.x) * 256 + col;

@@ -271,3 +271,13 @@ def check_scales_closed_forms(orc):
 
 
 ALL_CHECKS.append(check_scales_closed_forms)
+
+
+def check_zero_point_is_canonical(orc):
+    """A zero point is an integer code: a group whose minimum is 0 stores +0, not -0."""
+    W = np.abs(np.linspace(0.1, 1.0, 16, dtype=F32)).reshape(16, 1)
+    _, qs, qz = orc.pack(W, np.ones(16, dtype=F32), group_size=16, symmetric=False)
+    assert qz.view(np.uint16)[0, 0] == 0
+
+
+ALL_CHECKS.append(check_zero_point_is_canonical)
