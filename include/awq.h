@@ -110,6 +110,34 @@ AWQ_API awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t
                          float* mean_abs, void* ws, size_t ws_bytes, awq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The same statistic for callers that cannot allocate device memory.
+ * (No counterpart on the pages: this is a library convenience.)
+ *
+ * Some callers have no way to obtain a workspace: a plug-in running inside a
+ * host program that has already reserved all device memory for its own pool
+ * and exposes no allocator, or code on a latency-critical path that must not
+ * call cudaMalloc (which can synchronise the whole device).  This entry point
+ * takes only X and the output; its scratch (the per-row-slice partial sums)
+ * is a 4 MiB array of static device memory inside the library, which every
+ * device that loads the library holds until the process exits.
+ *
+ *   X, N, D_in, ldx, mean_abs  as for awq_act_stats
+ * Limits: D_in <= 1048576 channels (one row slice must fit the array);
+ * larger D_in returns AWQ_ERR_SHAPE without launching anything.  The call
+ * makes no cudaMalloc / cudaFree and uses no allocating library routine.
+ * The first call on a device looks up the array's device address for that
+ * device (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  Every call shares the one array: calls
+ * whose kernels overlap on the GPU (e.g. on two streams) race and corrupt
+ * each other's result, so serialise them.  Results equal awq_act_stats'
+ * whenever its row-slice plan fits the array, and agree to rounding
+ * otherwise.  There is no device status word: a non-finite X shows up as a
+ * non-finite entry of mean_abs.
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_act_stats_noalloc(const void* X, int64_t N, int64_t D_in, int64_t ldx,
+                                         float* mean_abs, awq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Steps 2-3: the alpha-grid scale search and its argmin.
  * "AWQ (Activation-aware Weight Quantization)", 缩放因子优化的完整流程 steps 3-6:
  * s_j(alpha) = activation_scale[j]^alpha, W' = diag(s) W, W4 per-group
