@@ -319,9 +319,13 @@ def run_ours(args, world, rank, local):
                 "algorithmic": f"2*N*D_in*D_out*G = {flops:.4g} flop per launch"}
     tp = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
     if os.path.exists(tp):
+        import hashlib
         with open(tp) as f:
             tj = json.load(f)
-        roofline["traffic"] = tj.get("search_gemm_dram_bytes_per_launch")
+        src = os.path.join(ROOT, tj.get("source", ""))
+        # counters count only while the kernel source is the one they were taken on
+        if os.path.isfile(src) and hashlib.sha1(open(src, "rb").read()).hexdigest() == tj.get("source_sha1"):
+            roofline["traffic"] = tj.get("search_gemm_dram_bytes_per_launch")
     launches = sum(KERNELS_PER_LAUNCHER.get(k, 1) * n for k, (n, _) in kern.items())
 
     # ---- end to end through the public API with host buffers
