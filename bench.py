@@ -20,9 +20,7 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +28,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "AWQ alpha-search TFLOP/s & layers/sec (21-pt grid) vs tensor-pipe peak; pack GB/s"
 KERNELS_PER_LAUNCHER = {"act_stats": 2, "scale_table": 1, "group_params": 1, "materialize": 1,
-                        "search_gemm": 1, "reduce_argmin": 3, "pack": 1}
+                        "search_gemm": 1, "search_fused": 1, "reduce_argmin": 3, "pack": 1}
+SEARCH_KERNELS = ("search_fused", "search_gemm")
 
 
 def parse_args(argv=None):
@@ -89,63 +88,148 @@ def measured_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
-class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during a region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+class _CtypesNvml:
+    """The few NVML calls the clock sampler needs, through ctypes (for hosts
+    without the pynvml module)."""
+    NVML_CLOCK_SM = 1
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+
+    def _ok(self, rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what} failed with NVML status {rc}")
+
+    def nvmlInit(self):
+        self._ok(self.lib.nvmlInit_v2(), "nvmlInit_v2")
+
+    def nvmlShutdown(self):
+        self.lib.nvmlShutdown()
+
+    def _handle(self, fn, arg):
+        h = self.c.c_void_p()
+        self._ok(getattr(self.lib, fn)(arg, self.c.byref(h)), fn)
+        return h
+
+    def nvmlDeviceGetHandleByUUID(self, uuid):
+        return self._handle("nvmlDeviceGetHandleByUUID", uuid.encode())
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        return self._handle("nvmlDeviceGetHandleByPciBusId_v2", bus.encode())
+
+    def nvmlDeviceGetHandleByIndex(self, i):
+        return self._handle("nvmlDeviceGetHandleByIndex_v2", self.c.c_uint(i))
+
+    def _uint(self, fn, h, *args):
+        v = self.c.c_uint()
+        self._ok(getattr(self.lib, fn)(h, *args, self.c.byref(v)), fn)
+        return v.value
+
+    def nvmlDeviceGetMaxClockInfo(self, h, t):
+        return self._uint("nvmlDeviceGetMaxClockInfo", h, self.c.c_int(t))
+
+    def nvmlDeviceGetClockInfo(self, h, t):
+        return self._uint("nvmlDeviceGetClockInfo", h, self.c.c_int(t))
+
+    def nvmlDeviceGetPowerUsage(self, h):
+        return self._uint("nvmlDeviceGetPowerUsage", h)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self.c.c_ulonglong()
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._ok(fn(h, self.c.byref(v)), "clock event reasons")
+        return v.value
+
+
+def _nvml():
+    try:
+        import pynvml
+        return pynvml
+    except ImportError:
+        return _CtypesNvml()
+
+
+class ClockSampler:
+    """SM clock, power and clock-event reasons sampled through NVML every few
+    milliseconds (a background thread) while the timed region runs."""
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40, "hw_power_brake": 0x80}
+
+    def __init__(self, cuda_index: int, period_s: float = 0.004):
+        self.cuda_index = cuda_index
+        self.period = period_s
+        self.samples = []
+        self.reasons = set()
+        self.sm_max = None
+        self.err = None
+        self._stop = None
+        self._thr = None
+        self._nvml = None
+
+    def _handle(self, nv):
+        import torch
+        try:
+            u = str(torch.cuda.get_device_properties(self.cuda_index).uuid)
+            return nv.nvmlDeviceGetHandleByUUID(u if u.startswith("GPU-") else "GPU-" + u)
+        except Exception:
+            pass
+        try:
+            pr = torch.cuda.get_device_properties(self.cuda_index)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+            return nv.nvmlDeviceGetHandleByPciBusId(bus)
+        except Exception:
+            pass
+        return nv.nvmlDeviceGetHandleByIndex(self.cuda_index)
 
     def __enter__(self):
+        import threading
         try:
-            fd, self.path = tempfile.mkstemp(prefix="awq_clocks_", suffix=".csv")
-            os.close(fd)
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=self.fh, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
-        except Exception:
-            self.proc = None
+            nv = _nvml()
+            nv.nvmlInit()
+            self._nvml = nv
+            h = self._handle(nv)
+            self.sm_max = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
+            self._stop = threading.Event()
+
+            def run():
+                while not self._stop.is_set():
+                    try:
+                        sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+                        pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+                        rs = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                        self.samples.append((float(sm), float(pw)))
+                        for name, bit in self.REASONS.items():
+                            if rs & bit:
+                                self.reasons.add(name)
+                    except Exception as e:  # keep timing even if one query fails
+                        self.err = str(e)
+                    self._stop.wait(self.period)
+
+            self._thr = threading.Thread(target=run, daemon=True)
+            self._thr.start()
+        except Exception as e:
+            self.err = str(e)
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        if self._thr is not None:
+            self._stop.set()
+            self._thr.join(timeout=5)
+        if self._nvml is not None:
             try:
-                self.proc.wait(timeout=5)
+                self._nvml.nvmlShutdown()
             except Exception:
-                self.proc.kill()
-            self.fh.close()
+                pass
 
     def summary(self):
-        if self.proc is None or not self.path or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
-                    power.append(float(parts[3]))
-                except ValueError:
-                    continue
-                for nm, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(nm)
-        os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.sm_max, "reasons": [f"unavailable: {self.err}"]}
+        sm = [a for a, _ in self.samples]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self.sm_max, "reasons": sorted(self.reasons),
+                "samples": len(sm), "source": "nvml" if not isinstance(self._nvml, _CtypesNvml) else "nvml (ctypes)", "power_w_max": max(b for _, b in self.samples)}
 
 
 def workload_bytes(w, G):
@@ -307,12 +391,13 @@ def run_ours(args, world, rank, local):
         n, tot = kern.get(name, (0, 0.0))
         return tot / n if n else None
 
-    gemm_ms = per_launch_ms("search_gemm")
+    search_name = next((k for k in SEARCH_KERNELS if k in kern), "search_fused")
+    gemm_ms = per_launch_ms(search_name)
     pack_ms = per_launch_ms("pack")
     stats_ms = per_launch_ms("act_stats")
     peaks, peak_src = measured_peaks()
     achieved = flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
-    roofline = {"kernel": "search_gemm", "bound": "tensor", "achieved": achieved,
+    roofline = {"kernel": search_name, "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"] if achieved else None,
                 "traffic": None, "peak_source": f"{peak_src} bf16 dense burst",
@@ -324,8 +409,9 @@ def run_ours(args, world, rank, local):
             tj = json.load(f)
         src = os.path.join(ROOT, tj.get("source", ""))
         # counters count only while the kernel source is the one they were taken on
-        if os.path.isfile(src) and hashlib.sha1(open(src, "rb").read()).hexdigest() == tj.get("source_sha1"):
-            roofline["traffic"] = tj.get("search_gemm_dram_bytes_per_launch")
+        if (tj.get("kernel") == search_name and os.path.isfile(src)
+                and hashlib.sha1(open(src, "rb").read()).hexdigest() == tj.get("source_sha1")):
+            roofline["traffic"] = tj.get("dram_bytes_per_launch")
     launches = sum(KERNELS_PER_LAUNCHER.get(k, 1) * n for k, (n, _) in kern.items())
 
     # ---- end to end through the public API with host buffers

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -28,6 +29,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // ---------------------------------------------------------------- device / driver state
 std::mutex g_mu;
 int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+int g_pairs[kMaxDevices];    // resident CTA pairs of the fused search (0 = not queried)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 awq_status check_device(int* dev_out) {
@@ -63,6 +65,28 @@ awq_status get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 }
 
 awq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA; }
+
+awq_status get_pairs(int dev, int* pairs) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_pairs[dev] == 0) {
+    int n = 0;
+    if (search_fused_max_pairs(&n) != cudaSuccess || n < 1) return AWQ_ERR_CUDA;
+    g_pairs[dev] = n;
+  }
+  *pairs = g_pairs[dev];
+  return AWQ_OK;
+}
+
+// Development comparison: AWQ_SEARCH_IMPL=materialized selects the path that
+// writes every candidate matrix to the workspace and runs a plain GEMM over it.
+bool materialized_search() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = std::getenv("AWQ_SEARCH_IMPL");
+    v = (e && std::strcmp(e, "materialized") == 0) ? 1 : 0;
+  }
+  return v == 1;
+}
 
 // ---------------------------------------------------------------- optional event timing
 struct ProfRecord {
@@ -138,20 +162,21 @@ SearchLayout search_layout(int64_t N, int64_t D_in, int64_t D_out, int G, int gr
   SearchLayout L;
   const size_t g = static_cast<size_t>(G);
   const size_t din = static_cast<size_t>(D_in), dout = static_cast<size_t>(D_out);
-  L.m_tiles = static_cast<int>((N + kGemmBM - 1) / kGemmBM);
+  const bool mat = materialized_search();
+  L.m_tiles = mat ? static_cast<int>((N + kGemmBM - 1) / kGemmBM) : search_fused_m_tiles(N);
   size_t off = kHeaderBytes;
   L.s_tab = off;
   off = align_up(off + g * din * 4, 256);
   L.r_tab = off;
   off = align_up(off + g * din * 4, 256);
   L.qp = off;
-  off = align_up(off + g * (din / group_size) * dout * sizeof(QParam), 256);
+  off = align_up(off + qparam_floats(G, D_in / group_size, D_out) * 4, 256);
   L.partial = off;
   off = align_up(off + g * static_cast<size_t>(L.m_tiles) * dout * 4, 256);
   L.col = off;
   off = align_up(off + g * dout * 8, 256);
   L.dW = off;
-  off = align_up(off + g * din * dout * 2, 256);
+  if (mat) off = align_up(off + g * din * dout * 2, 256);
   L.total = off;
   return L;
 }
@@ -252,18 +277,25 @@ awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int
     return AWQ_ERR_ALIGNMENT;
   const SearchLayout L = search_layout(N, D_in, D_out, G, cfg->group_size);
   if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
-  st = check_device(nullptr);
+  int dev = 0;
+  st = check_device(&dev);
   if (st != AWQ_OK) return st;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   st = get_encode(&encode);
   if (st != AWQ_OK) return st;
+  const bool mat = materialized_search();
+  int pairs = 0;
+  if (!mat) {
+    st = get_pairs(dev, &pairs);
+    if (st != AWQ_OK) return st;
+  }
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
   uint32_t* status = status_word(ws);
   float* s_tab = reinterpret_cast<float*>(base + L.s_tab);
   float* r_tab = reinterpret_cast<float*>(base + L.r_tab);
-  QParam* qp = reinterpret_cast<QParam*>(base + L.qp);
+  float* qp = reinterpret_cast<float*>(base + L.qp);
   float* partial = reinterpret_cast<float*>(base + L.partial);
   double* col = col_losses ? col_losses : reinterpret_cast<double*>(base + L.col);
   void* dW = base + L.dW;
@@ -278,13 +310,19 @@ awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int
     ProfScope prof("group_params", s);
     e = launch_group_params(W, s_tab, D_in, D_out, G, cfg->group_size, cfg->symmetric, qp, status, s);
   }
-  if (e == cudaSuccess) {
-    ProfScope prof("materialize", s);
-    e = launch_materialize(W, s_tab, r_tab, qp, D_in, D_out, G, cfg->group_size, cfg->symmetric, dW, s);
-  }
-  if (e == cudaSuccess) {
-    ProfScope prof("search_gemm", s);
-    e = launch_gemm_ssq(encode, X, dW, N, D_out, D_in, G, partial, status, s);
+  if (mat) {
+    if (e == cudaSuccess) {
+      ProfScope prof("materialize", s);
+      e = launch_materialize(W, s_tab, r_tab, qp, D_in, D_out, G, cfg->group_size, cfg->symmetric, dW, s);
+    }
+    if (e == cudaSuccess) {
+      ProfScope prof("search_gemm", s);
+      e = launch_gemm_ssq(encode, X, dW, N, D_out, D_in, G, partial, status, s);
+    }
+  } else if (e == cudaSuccess) {
+    ProfScope prof("search_fused", s);
+    e = launch_search_fused(encode, X, W, s_tab, r_tab, qp, N, D_in, D_out, G, cfg->group_size, cfg->symmetric,
+                            partial, status, pairs, s);
   }
   if (e == cudaSuccess) {
     ProfScope prof("reduce_argmin", s);

@@ -27,17 +27,26 @@ struct AlphaGrid {
   double a[kMaxGrid];
 };
 
-// Per (candidate, group, column) quantiser parameters used by the search:
+// Quantiser parameters of one (candidate, group, column) used by the search:
 //   inv = 1/step (0 for a zero step), zm = 1.5*2^23 + zero, step.
 struct QParam {
   float inv, zm, step, pad;
 };
+// In memory they are stored per (candidate, group) in chunks of 8 output
+// columns: {inv x8, zm x8, step x8, 4 unused} = 28 floats (112 bytes).  The
+// 112-byte stride spreads the 8 chunks read by 8 neighbouring producer
+// threads over all 32 shared-memory banks.
+constexpr int kQChunkCols = 8;
+constexpr int kQChunkFloats = 28;
+inline size_t qparam_floats(int G, int64_t T, int64_t D_out) {
+  return static_cast<size_t>(G) * static_cast<size_t>(T) * static_cast<size_t>(D_out / kQChunkCols) * kQChunkFloats;
+}
 
 cudaError_t launch_scale_table(const float* mean_abs, int64_t D_in, const AlphaGrid& grid, int G, float act_floor,
                                float* s_tab, float* r_tab, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in, int64_t D_out, int G,
-                                int group_size, int symmetric, QParam* qp, uint32_t* status, cudaStream_t stream);
-cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r_tab, const QParam* qp,
+                                int group_size, int symmetric, float* qp, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r_tab, const float* qp,
                                int64_t D_in, int64_t D_out, int G, int group_size, int symmetric, void* dW,
                                cudaStream_t stream);
 cudaError_t launch_pack(const void* W, const float* s, int64_t D_in, int64_t D_out, int group_size, int symmetric,
@@ -55,6 +64,16 @@ cudaError_t launch_gemm_ssq(PFN_cuTensorMapEncodeTiled_v12000 encode, const void
 // Plain C = A * B in fp32 (self-test of the tensor-core main loop).
 cudaError_t launch_gemm_store(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* A, const void* B, int b_mn_major,
                               int64_t M, int64_t N, int64_t K, float* C, uint32_t* status, cudaStream_t stream);
+
+// ----------------------------------------------------------------- fused search (CTA pairs)
+// Rows of X per partial-sum slot of the fused search: [G][m_tiles][D_out].
+int search_fused_m_tiles(int64_t N);
+// CTA pairs that fit on the device at once (occupancy query).
+cudaError_t search_fused_max_pairs(int* pairs);
+cudaError_t launch_search_fused(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, const void* W,
+                                const float* s_tab, const float* r_tab, const float* qp, int64_t N, int64_t D_in,
+                                int64_t D_out, int G, int group_size, int symmetric, float* partial,
+                                uint32_t* status, int max_pairs, cudaStream_t stream);
 
 // ----------------------------------------------------------------- reductions
 cudaError_t launch_reduce_losses(const float* partial, int m_tiles, int64_t D_out, int G, double* col_losses,

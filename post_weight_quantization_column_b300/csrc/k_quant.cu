@@ -84,7 +84,7 @@ template <int GS>
 __global__ void __launch_bounds__(128) group_params_kernel(const __nv_bfloat16* __restrict__ W,
                                                          const float* __restrict__ s_tab, int64_t D_in,
                                                          int64_t D_out, int G, int symmetric,
-                                                         QParam* __restrict__ qp, uint32_t* status) {
+                                                         float* __restrict__ qp, uint32_t* status) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* wsh = reinterpret_cast<uint32_t*>(smem);             // [GS][128] bf16 pairs
   float* ssh = reinterpret_cast<float*>(smem + GS * 128 * 4);    // [G][GS]
@@ -136,9 +136,17 @@ __global__ void __launch_bounds__(128) group_params_kernel(const __nv_bfloat16* 
       }
     }
     if (n < D_out) {
-      QParam* dst = qp + (static_cast<int64_t>(k) * T + grp) * D_out + n;
-      dst[0] = make_qparam(lo0, hi0, symmetric, status);
-      dst[1] = make_qparam(lo1, hi1, symmetric, status);
+      // n is even, so both columns sit in one 8-column chunk
+      float* dst = qp + ((static_cast<int64_t>(k) * T + grp) * (D_out / kQChunkCols) + n / kQChunkCols) * kQChunkFloats +
+                   (n % kQChunkCols);
+      const QParam q0 = make_qparam(lo0, hi0, symmetric, status);
+      const QParam q1 = make_qparam(lo1, hi1, symmetric, status);
+      dst[0] = q0.inv;
+      dst[1] = q1.inv;
+      dst[kQChunkCols] = q0.zm;
+      dst[kQChunkCols + 1] = q1.zm;
+      dst[2 * kQChunkCols] = q0.step;
+      dst[2 * kQChunkCols + 1] = q1.step;
     }
   }
 }
@@ -146,7 +154,7 @@ __global__ void __launch_bounds__(128) group_params_kernel(const __nv_bfloat16* 
 static size_t group_params_smem(int GS, int G) { return static_cast<size_t>(GS) * 512 + static_cast<size_t>(G) * GS * 4; }
 
 cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in, int64_t D_out, int G,
-                                int group_size, int symmetric, QParam* qp, uint32_t* status, cudaStream_t stream) {
+                                int group_size, int symmetric, float* qp, uint32_t* status, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>((D_out + 255) / 256), static_cast<unsigned>(D_in / group_size));
   const size_t smem = group_params_smem(group_size, G);
   const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
@@ -193,7 +201,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 __global__ void __launch_bounds__(256) materialize_kernel(const __nv_bfloat16* __restrict__ W,
                                                         const float* __restrict__ s_tab,
                                                         const float* __restrict__ r_tab,
-                                                        const QParam* __restrict__ qp, int64_t D_in, int64_t D_out,
+                                                        const float* __restrict__ qp, int64_t D_in, int64_t D_out,
                                                         int group_size, float lo, float hi,
                                                         __nv_bfloat16* __restrict__ dW) {
   const int lane = threadIdx.x & 31;
@@ -204,10 +212,10 @@ __global__ void __launch_bounds__(256) materialize_kernel(const __nv_bfloat16* _
   const int64_t jb = static_cast<int64_t>(blockIdx.y) * 64;
   const int64_t T = D_in / group_size;
   const int64_t grp = jb / group_size;
-  const QParam* q = qp + (static_cast<int64_t>(k) * T + grp) * D_out + n;
+  const float* q = qp + ((static_cast<int64_t>(k) * T + grp) * (D_out / kQChunkCols) + n / kQChunkCols) * kQChunkFloats;
   QParam qv[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) qv[c] = q[c];
+  for (int c = 0; c < 8; ++c) qv[c] = QParam{q[c], q[kQChunkCols + c], q[2 * kQChunkCols + c], 0.f};
 #pragma unroll 2
   for (int i = 0; i < 8; ++i) {
     const int64_t j = jb + rl + 8 * i;
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(256) materialize_kernel(const __nv_bfloat16* _
   }
 }
 
-cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r_tab, const QParam* qp,
+cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r_tab, const float* qp,
                                int64_t D_in, int64_t D_out, int G, int group_size, int symmetric, void* dW,
                                cudaStream_t stream) {
   const float lo = symmetric ? kMagic - 7.f : kMagic;

@@ -1,0 +1,529 @@
+// Fused candidate search on a tcgen05 CTA pair (sm_103a).
+//
+// For candidate k the search needs the output error of the quantised layer,
+//   E_k = X * S_k^-1 W'hat_k - X * W = X * D_k,  D_k = S_k^-1 W'hat_k - W,
+// and only the per-column sums of squares of E_k ("AWQ (Activation-aware
+// Weight Quantization)", 缩放因子优化的完整流程 steps 3-4: scale, quantise
+// per group, dequantise, L = ||X S^-1 W'hat - X W||^2).  D_k is never stored:
+// producer warps build each bf16 tile of it in registers from W, the scale
+// row s_k and the per-group step / zero, and write it straight into the
+// shared-memory operand layout of the tensor cores.
+//
+// Work unit: (candidate k, 512 rows of X, 256 columns of W).  Two CTAs of a
+// cluster form a tcgen05 pair: each holds two stacked 128-row subtiles of X
+// (rows m0 + 256*s + 128*rank) and produces half (128 columns) of the D_k
+// tile; the even CTA issues M256 x N256 x K16 MMAs that read A from both CTAs
+// and B from both halves, accumulating in fp32 TMEM (2 subtiles x 256
+// columns = all 512 TMEM columns of each CTA).  Every produced element of D_k
+// feeds 512 rows of MMA work, which keeps the producer's CUDA-core cost well
+// under the tensor-core time of the same K step.
+//
+// Roles (640 threads per CTA):
+//   warp 0      TMA: X subtiles (K-major, 128-byte swizzle) per K step; the
+//               completion is counted on the even CTA's barrier
+//   warp 1      TMEM allocation; in the even CTA the single-thread MMA issuer
+//   warp 2      TMA: producer inputs per K step (W tile, s and 1/s slices,
+//               step / zero of the group) into a separate ring
+//   warps 4-11  epilogue: TMEM -> registers, square, column sums over the
+//               CTA's 256 rows (fixed order), one fp32 partial per column
+//   warps 12-19 producers (256 threads, 8 columns x 4 rows each per K step)
+// The kernel is persistent: each pair walks the work units with a stride of
+// the number of pairs.  Every mbarrier wait is bounded; a timeout records
+// AWQ_ERR_TIMEOUT and every role leaves its loop.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace awqdev {
+namespace {
+
+constexpr int kBK = 64;                        // K (input rows of W) per step
+constexpr int kSubRows = 128;                  // X rows of one subtile in one CTA
+constexpr int kStack = 2;                      // stacked subtiles per CTA
+constexpr int kPairN = 256;                    // columns of W per work unit
+constexpr int kHalfN = kPairN / 2;             // columns produced by one CTA
+constexpr int kStages = 3;                     // X / D ring
+constexpr int kWStages = 3;                    // producer-input ring
+constexpr int kASubBytes = kSubRows * kBK * 2;  // 16 KB
+constexpr int kABytes = kStack * kASubBytes;    // 32 KB
+constexpr int kBBytes = kBK * kHalfN * 2;       // 16 KB: 64 K x 128 N bf16, N-major, 128B swizzle
+constexpr int kWTileBytes = kBK * kHalfN * 2;   // 16 KB: 64 rows x 128 columns bf16 (two 64-column boxes)
+constexpr int kSBytes = kBK * 4;                // s slice
+constexpr int kQBytes = (kHalfN / kQChunkCols) * kQChunkFloats * 4;  // step / zero chunks of 128 columns
+constexpr int kWStageTx = kWTileBytes + 2 * kSBytes + kQBytes;
+constexpr int kWStageStride = 19 * 1024;
+constexpr int kOffB = kStages * kABytes;
+constexpr int kOffW = kOffB + kStages * kBBytes;
+constexpr int kSmemBytes = kOffW + kWStages * kWStageStride;
+constexpr int kTmemCols = 512;
+constexpr int kThreads = 640;
+constexpr int kEpiWarp0 = 4, kEpiWarps = 8;
+constexpr int kProdWarp0 = 12, kProdWarps = 8;
+constexpr int kFullCount = 1 + 2 * kProdWarps;   // TMA expect-tx + producer warps of both CTAs
+constexpr int kAccEmptyCount = 2 * kEpiWarps;
+
+static_assert(kWTileBytes + 2 * kSBytes + kQBytes <= kWStageStride, "W stage");
+static_assert(kSmemBytes + 1024 <= 227 * 1024, "shared memory");
+
+struct FusedArgs {
+  int N, D_in, D_out, G, T, group_size;
+  int m_blocks, n_blocks, num_tiles, m_tiles;
+  float clamp_lo, clamp_hi;
+  float* partial;  // [G][m_tiles][D_out]
+  uint32_t* status;
+};
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Sum v[0..31] across the 32 lanes so that lane l ends with sum_lanes v[l].
+__device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+    }
+  }
+  return v[0];
+}
+
+struct Tile {
+  int k, m_blk, n_blk;
+};
+__device__ __forceinline__ Tile decode_tile(int t, const FusedArgs& p) {
+  Tile r;
+  r.k = t % p.G;
+  const int rest = t / p.G;
+  r.n_blk = rest % p.n_blocks;
+  r.m_blk = rest / p.n_blocks;
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    search_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmR,
+                        const __grid_constant__ CUtensorMap tmQ, FusedArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kStages];    // used in the even CTA only
+  __shared__ __align__(8) uint64_t empty_bar[kStages];   // both CTAs, one arrival by the MMA commit
+  __shared__ __align__(8) uint64_t wfull_bar[kWStages];
+  __shared__ __align__(8) uint64_t wempty_bar[kWStages];
+  __shared__ __align__(8) uint64_t acc_full_bar;         // both CTAs
+  __shared__ __align__(8) uint64_t acc_empty_bar;        // even CTA
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ float red[4][kPairN];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(nclusters_x());
+  const int KB = p.D_in / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], kFullCount);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(&wfull_bar[s], 1);
+      mbar_init(&wempty_bar[s], kProdWarps);
+    }
+    mbar_init(&acc_full_bar, 1);
+    mbar_init(&acc_empty_bar, kAccEmptyCount);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 32 * 2) {
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmS);
+    prefetch_tmap(&tmR);
+    prefetch_tmap(&tmQ);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tmem_base_sh, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  volatile int* abort_flag = &abort_sh;
+
+  // shared::cluster addresses of the even CTA's barriers
+  const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);
+  const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty_bar), 0);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- X loader
+    if (lane == 0) {
+      int it = 0;
+      for (int t = pair; t < p.num_tiles && !*abort_flag; t += npairs) {
+        const Tile tl = decode_tile(t, p);
+        const int row0 = tl.m_blk * (2 * kStack * kSubRows) + static_cast<int>(rank) * kSubRows;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (it >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1, p.status, abort_flag)) break;
+          if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * kABytes);
+          const uint32_t bar = full0 + static_cast<uint32_t>(s) * 8u;
+#pragma unroll
+          for (int sub = 0; sub < kStack; ++sub)
+            tma_load_2d_pair(smem + s * kABytes + sub * kASubBytes, &tmX, bar, kb * kBK,
+                             row0 + sub * 2 * kSubRows);
+        }
+        if (*abort_flag) break;
+      }
+      // drain: the MMA commits of the last steps arrive on this CTA's empty
+      // barriers; wait for them so that no arrival targets an exited CTA
+      const int first = it - kStages < 0 ? 0 : it - kStages;
+      for (int j = first; j < it; ++j)
+        mbar_wait_cluster(&empty_bar[j % kStages], (j / kStages) & 1, p.status, abort_flag);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      // M = 256 (pair), N = 256, bf16 x bf16 -> fp32, A K-major, B N-major
+      constexpr uint32_t idesc = idesc_bf16_f32(256, kPairN, 0, 1);
+      int it = 0, tc = 0;
+      for (int t = pair; t < p.num_tiles; t += npairs, ++tc) {
+        if (tc > 0 && !mbar_wait_cluster(&acc_empty_bar, (tc - 1) & 1, p.status, abort_flag)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!mbar_wait_cluster(&full_bar[s], ph, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * kABytes);
+          const uint32_t b_addr = smem_u32(smem + kOffB + s * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // B: N-major SW128; 64-column chunks 8 KB apart (LBO), 8-row K
+            // groups 1024 B apart (SBO); a K step of 16 is two K groups.
+            const uint64_t bd = sdesc_sw128(b_addr + kk * 2048, kBK * 128, 1024);
+#pragma unroll
+            for (int sub = 0; sub < kStack; ++sub) {
+              const uint64_t ad = sdesc_sw128(a_addr + sub * kASubBytes + kk * 32, 16, 1024);
+              umma_bf16_pair(tmem + static_cast<uint32_t>(sub * kPairN), ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+          }
+          umma_commit_pair_mc(&empty_bar[s], 0x3);
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(&acc_full_bar, 0x3);
+      }
+      // the epilogues' last arrivals (some remote) land before the pair exits
+      if (tc > 0 && !*abort_flag) mbar_wait_cluster(&acc_empty_bar, (tc - 1) & 1, p.status, abort_flag);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------- producer-input loader
+    if (lane == 0) {
+      int wit = 0;
+      for (int t = pair; t < p.num_tiles && !*abort_flag; t += npairs) {
+        const Tile tl = decode_tile(t, p);
+        const int n_base = tl.n_blk * kPairN + static_cast<int>(rank) * kHalfN;
+        for (int kb = 0; kb < KB; ++kb, ++wit) {
+          const int s = wit % kWStages;
+          const uint32_t ph = (wit / kWStages) & 1;
+          if (wit >= kWStages && !mbar_wait(&wempty_bar[s], ph ^ 1, p.status, abort_flag)) break;
+          uint8_t* st = smem + kOffW + s * kWStageStride;
+          mbar_arrive_expect_tx(&wfull_bar[s], kWStageTx);
+          tma_load_2d(st, &tmW, &wfull_bar[s], n_base, kb * kBK);
+          tma_load_2d(st + kWTileBytes / 2, &tmW, &wfull_bar[s], n_base + 64, kb * kBK);
+          tma_load_2d(st + kWTileBytes, &tmS, &wfull_bar[s], kb * kBK, tl.k);
+          tma_load_2d(st + kWTileBytes + kSBytes, &tmR, &wfull_bar[s], kb * kBK, tl.k);
+          tma_load_3d(st + kWTileBytes + 2 * kSBytes, &tmQ, &wfull_bar[s], 0, n_base / kQChunkCols,
+                      tl.k * p.T + (kb * kBK) / p.group_size);
+        }
+        if (*abort_flag) break;
+      }
+      // drain loads still in flight into this CTA
+      const int first = wit - kWStages < 0 ? 0 : wit - kWStages;
+      for (int j = first; j < wit; ++j) mbar_wait(&wfull_bar[j % kWStages], (j / kWStages) & 1, nullptr, nullptr);
+    }
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+    // ---------------------------------------------------------- epilogue
+    const int e = warp - kEpiWarp0;
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int ch = e >> 2;          // column half: [ch*128, ch*128 + 128)
+    const int ecol = e * 32 + lane; // column of the final fixed-order sum
+    int tc = 0;
+    for (int t = pair; t < p.num_tiles; t += npairs, ++tc) {
+      const Tile tl = decode_tile(t, p);
+      bool ok = mbar_wait(&acc_full_bar, tc & 1, p.status, abort_flag);
+      tc_fence_after();
+      if (ok) {
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          const int col = ch * 128 + cc * 32;
+          float a[32], b[32];
+          tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(col), a);
+          tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kPairN + col), b);
+          if (cc == 3) {
+            // every TMEM read of this warp is complete: release the accumulator
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty0);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = fmaf(a[i], a[i], b[i] * b[i]);
+          red[q][col + lane] = transpose_sum32(a, lane);
+        }
+      }
+      if (named_bar_or(1, kEpiWarps * 32, !ok || *abort_flag)) break;
+      {
+        const float sum = ((red[0][ecol] + red[1][ecol]) + red[2][ecol]) + red[3][ecol];
+        const int n = tl.n_blk * kPairN + ecol;
+        const int mt = 2 * tl.m_blk + static_cast<int>(rank);
+        if (n < p.D_out) p.partial[(static_cast<int64_t>(tl.k) * p.m_tiles + mt) * p.D_out + n] = sum;
+      }
+      named_bar_sync(1, kEpiWarps * 32);
+    }
+  } else if (warp >= kProdWarp0) {
+    // ---------------------------------------------------------- producers
+    // thread: 8 columns (chunk c) x 4 rows (4*rg .. 4*rg+3) of the 64 x 128 tile
+    const int pt = threadIdx.x - kProdWarp0 * 32;
+    const int c = pt & 15;
+    const int rg = pt >> 4;
+    const int h = c >> 3;        // 64-column half of the CTA's 128 columns
+    const int c8 = c & 7;        // 16-byte chunk inside a 128-byte row
+    const float lo = p.clamp_lo, hi = p.clamp_hi;
+    const uint32_t full_mine = full0;  // even CTA's full barriers (cluster address)
+    int it = 0, wit = 0;
+    for (int t = pair; t < p.num_tiles && !*abort_flag; t += npairs) {
+      const Tile tl = decode_tile(t, p);
+      int cached_group = -1;
+      float2 inv2[4], zm2[4], nzm2[4], nstep2[4];
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb, ++it, ++wit) {
+        const int ws = wit % kWStages;
+        if (!mbar_wait(&wfull_bar[ws], (wit / kWStages) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int s = it % kStages;
+        const uint8_t* st = smem + kOffW + ws * kWStageStride;
+        const int grp = (kb * kBK) / p.group_size;
+        if (grp != cached_group) {
+          cached_group = grp;
+          // chunk c: {1/step x8, 1.5*2^23 + zero x8, step x8, unused x4}
+          const float4* qp = reinterpret_cast<const float4*>(st + kWTileBytes + 2 * kSBytes + c * (kQChunkFloats * 4));
+          const float4 i0 = qp[0], i1 = qp[1], z0 = qp[2], z1 = qp[3], s0 = qp[4], s1 = qp[5];
+          inv2[0] = make_float2(i0.x, i0.y);
+          inv2[1] = make_float2(i0.z, i0.w);
+          inv2[2] = make_float2(i1.x, i1.y);
+          inv2[3] = make_float2(i1.z, i1.w);
+          zm2[0] = make_float2(z0.x, z0.y);
+          zm2[1] = make_float2(z0.z, z0.w);
+          zm2[2] = make_float2(z1.x, z1.y);
+          zm2[3] = make_float2(z1.z, z1.w);
+          nstep2[0] = make_float2(-s0.x, -s0.y);
+          nstep2[1] = make_float2(-s0.z, -s0.w);
+          nstep2[2] = make_float2(-s1.x, -s1.y);
+          nstep2[3] = make_float2(-s1.z, -s1.w);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) nzm2[j] = make_float2(-zm2[j].x, -zm2[j].y);
+        }
+        const float4 s4 = *reinterpret_cast<const float4*>(st + kWTileBytes + rg * 16);
+        const float4 r4 = *reinterpret_cast<const float4*>(st + kWTileBytes + kSBytes + rg * 16);
+        const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+        const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
+        uint32_t o[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = rg * 4 + i;
+          const uint4 wv = *reinterpret_cast<const uint4*>(st + h * (kWTileBytes / 2) + row * 128 + c8 * 16);
+          const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+          const float2 s2 = make_float2(sv[i], sv[i]);
+          const float2 r2 = make_float2(rv[i], rv[i]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // w' = w s;  t = rint(w'/step) + zero (held as 1.5*2^23 + code);
+            // clamp to the code range; the negated difference
+            // (w' - (code - zero) step) / s = W - S^-1 W'hat (its squares
+            // give the same loss)
+            const float2 w2 = make_float2(bf16lo(wu[j]), bf16hi(wu[j]));
+            const float2 wp = __fmul2_rn(w2, s2);
+            float2 tq = __ffma2_rn(wp, inv2[j], zm2[j]);
+            tq.x = fminf(fmaxf(tq.x, lo), hi);
+            tq.y = fminf(fmaxf(tq.y, lo), hi);
+            const float2 qz = __fadd2_rn(tq, nzm2[j]);
+            const float2 ev = __ffma2_rn(qz, nstep2[j], wp);
+            const float2 d = __fmul2_rn(ev, r2);
+            o[i][j] = pack_bf16x2(d.x, d.y);
+          }
+        }
+        // every input of this stage is in registers: free it for the loader
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wempty_bar[ws]);
+        // the operand slot is reused once the MMAs that read it 3 steps ago completed
+        if (it >= kStages && !mbar_wait_cluster(&empty_bar[s], ((it / kStages) & 1) ^ 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* bst = smem + kOffB + s * kBBytes + h * (kBK * 128);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = rg * 4 + i;
+          *reinterpret_cast<uint4*>(bst + row * 128 + ((c8 ^ (row & 7)) * 16)) =
+              make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(full_mine + static_cast<uint32_t>(s) * 8u);
+      }
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no arrival or MMA of one CTA may target an exited peer
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+cudaError_t encode_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, CUtensorMapDataType dt,
+                       int rank, const void* base, const cuuint64_t* dims, const cuuint64_t* strides,
+                       const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int search_fused_m_tiles(int64_t N) {
+  return static_cast<int>(2 * ((N + 2 * kStack * kSubRows - 1) / (2 * kStack * kSubRows)));
+}
+
+cudaError_t launch_search_fused(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, const void* W,
+                                const float* s_tab, const float* r_tab, const float* qp, int64_t N, int64_t D_in,
+                                int64_t D_out, int G, int group_size, int symmetric, float* partial,
+                                uint32_t* status, int max_pairs, cudaStream_t stream) {
+  CUtensorMap tmX, tmW, tmS, tmR, tmQ;
+  cudaError_t e;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D_in), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D_in) * 2};
+    const cuuint32_t box[2] = {kBK, kSubRows};
+    e = encode_map(encode, &tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D_out), static_cast<cuuint64_t>(D_in)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D_out) * 2};
+    const cuuint32_t box[2] = {64, kBK};
+    e = encode_map(encode, &tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D_in), static_cast<cuuint64_t>(G)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D_in) * 4};
+    const cuuint32_t box[2] = {kBK, 1};
+    e = encode_map(encode, &tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, s_tab, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    e = encode_map(encode, &tmR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, r_tab, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  const int T = static_cast<int>(D_in / group_size);
+  {
+    const cuuint64_t chunks = static_cast<cuuint64_t>(D_out / kQChunkCols);
+    const cuuint64_t dims[3] = {kQChunkFloats, chunks, static_cast<cuuint64_t>(G) * T};
+    const cuuint64_t strides[2] = {kQChunkFloats * 4, chunks * kQChunkFloats * 4};
+    const cuuint32_t box[3] = {kQChunkFloats, kHalfN / kQChunkCols, 1};
+    e = encode_map(encode, &tmQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, qp, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  FusedArgs a;
+  a.N = static_cast<int>(N);
+  a.D_in = static_cast<int>(D_in);
+  a.D_out = static_cast<int>(D_out);
+  a.G = G;
+  a.T = T;
+  a.group_size = group_size;
+  a.m_blocks = static_cast<int>((N + 2 * kStack * kSubRows - 1) / (2 * kStack * kSubRows));
+  a.n_blocks = static_cast<int>((D_out + kPairN - 1) / kPairN);
+  a.num_tiles = G * a.m_blocks * a.n_blocks;
+  a.m_tiles = 2 * a.m_blocks;
+  constexpr float kMagic = 12582912.0f;
+  a.clamp_lo = symmetric ? kMagic - 7.f : kMagic;
+  a.clamp_hi = symmetric ? kMagic + 7.f : kMagic + 15.f;
+  a.partial = partial;
+  a.status = status;
+
+  const size_t smem = static_cast<size_t>(kSmemBytes) + 1024;
+  e = cudaFuncSetAttribute(search_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int pairs = max_pairs;
+  if (pairs > a.num_tiles) pairs = a.num_tiles;
+  if (pairs < 1) pairs = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, search_fused_kernel, tmX, tmW, tmS, tmR, tmQ, a);
+}
+
+// Number of CTA pairs that can be resident at once (one pair per two SMs).
+cudaError_t search_fused_max_pairs(int* pairs) {
+  const size_t smem = static_cast<size_t>(kSmemBytes) + 1024;
+  cudaError_t e =
+      cudaFuncSetAttribute(search_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, search_fused_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  *pairs = n;
+  return cudaSuccess;
+}
+
+}  // namespace awqdev
