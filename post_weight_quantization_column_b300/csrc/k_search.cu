@@ -26,7 +26,8 @@
 //               step / zero of the group) into a separate ring
 //   warps 4-11  epilogue: TMEM -> registers, square, column sums over the
 //               CTA's 256 rows (fixed order), one fp32 partial per column
-//   warps 12-19 producers (256 threads, 8 columns x 4 rows each per K step)
+//   warps 12-19 producers: two groups of 4 warps on alternate K steps
+//               (128 threads, 8 columns x 8 rows each per step)
 // The kernel is persistent: each pair walks the work units with a stride of
 // the number of pairs.  Every mbarrier wait is bounded; a timeout records
 // AWQ_ERR_TIMEOUT and every role leaves its loop.
@@ -60,7 +61,8 @@ constexpr int kTmemCols = 512;
 constexpr int kThreads = 640;
 constexpr int kEpiWarp0 = 4, kEpiWarps = 8;
 constexpr int kProdWarp0 = 12, kProdWarps = 8;
-constexpr int kFullCount = 1 + 2 * kProdWarps;   // TMA expect-tx + producer warps of both CTAs
+constexpr int kGroupWarps = 4;                   // producer warps per K step (two groups alternate)
+constexpr int kFullCount = 1 + 2 * kGroupWarps;  // TMA expect-tx + one producer group of each CTA
 constexpr int kAccEmptyCount = 2 * kEpiWarps;
 
 static_assert(kWTileBytes + 2 * kSBytes + kQBytes <= kWStageStride, "W stage");
@@ -94,6 +96,37 @@ __device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
     }
   }
   return v[0];
+}
+
+// Four rows x 8 columns of the negated difference tile D = W - S^-1 W'hat:
+//   w' = w s;  t = rint(w' / step) + zero, held as 1.5*2^23 + code;  clamp
+//   to the code range;  d = (w' - (code - zero) step) / s.
+// (D and -D give the same loss.)  `w` points at row 0 (16 bytes of 8 bf16),
+// rows 128 bytes apart; s4 / r4 hold s and 1/s of the 4 rows.
+__device__ __forceinline__ void produce4(const uint8_t* w, float4 s4, float4 r4, const float2 (&inv2)[4],
+                                         const float2 (&zm2)[4], const float2 (&nzm2)[4], const float2 (&nstep2)[4],
+                                         float lo, float hi, uint32_t (&o)[4][4]) {
+  const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+  const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 wv = *reinterpret_cast<const uint4*>(w + i * 128);
+    const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+    const float2 s2 = make_float2(sv[i], sv[i]);
+    const float2 r2 = make_float2(rv[i], rv[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 w2 = make_float2(bf16lo(wu[j]), bf16hi(wu[j]));
+      const float2 wp = __fmul2_rn(w2, s2);
+      float2 tq = __ffma2_rn(wp, inv2[j], zm2[j]);
+      tq.x = fminf(fmaxf(tq.x, lo), hi);
+      tq.y = fminf(fmaxf(tq.y, lo), hi);
+      const float2 qz = __fadd2_rn(tq, nzm2[j]);
+      const float2 ev = __ffma2_rn(qz, nstep2[j], wp);
+      const float2 d = __fmul2_rn(ev, r2);
+      o[i][j] = pack_bf16x2(d.x, d.y);
+    }
+  }
 }
 
 struct Tile {
@@ -139,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(&wfull_bar[s], 1);
-      mbar_init(&wempty_bar[s], kProdWarps);
+      mbar_init(&wempty_bar[s], kGroupWarps);
     }
     mbar_init(&acc_full_bar, 1);
     mbar_init(&acc_empty_bar, kAccEmptyCount);
@@ -282,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // every TMEM read of this warp is complete: release the accumulator
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty0);
+            if (lane == 0) mbar_arrive_remote(acc_empty0);
           }
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = fmaf(a[i], a[i], b[i] * b[i]);
@@ -300,23 +333,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kProdWarp0) {
     // ---------------------------------------------------------- producers
-    // thread: 8 columns (chunk c) x 4 rows (4*rg .. 4*rg+3) of the 64 x 128 tile
-    const int pt = threadIdx.x - kProdWarp0 * 32;
-    const int c = pt & 15;
-    const int rg = pt >> 4;
+    // Two groups of 4 warps take alternate K steps, so that one group's
+    // waits overlap the other's arithmetic.  Thread: 8 columns (chunk c) x 8
+    // rows (8*rg .. 8*rg+7) of the 64 x 128 tile of its step.
+    const int grp_id = (warp - kProdWarp0) / kGroupWarps;
+    const int gt = threadIdx.x - (kProdWarp0 + grp_id * kGroupWarps) * 32;
+    const int c = gt & 15;
+    const int rg = gt >> 4;
     const int h = c >> 3;        // 64-column half of the CTA's 128 columns
     const int c8 = c & 7;        // 16-byte chunk inside a 128-byte row
     const float lo = p.clamp_lo, hi = p.clamp_hi;
-    const uint32_t full_mine = full0;  // even CTA's full barriers (cluster address)
-    int it = 0, wit = 0;
+    int it = 0;
     for (int t = pair; t < p.num_tiles && !*abort_flag; t += npairs) {
-      const Tile tl = decode_tile(t, p);
       int cached_group = -1;
       float2 inv2[4], zm2[4], nzm2[4], nstep2[4];
       bool ok = true;
-      for (int kb = 0; kb < KB; ++kb, ++it, ++wit) {
-        const int ws = wit % kWStages;
-        if (!mbar_wait(&wfull_bar[ws], (wit / kWStages) & 1, p.status, abort_flag)) {
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        if ((it & 1) != grp_id) continue;
+        const int ws = it % kWStages;
+        if (!mbar_wait(&wfull_bar[ws], (it / kWStages) & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
@@ -343,53 +378,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) nzm2[j] = make_float2(-zm2[j].x, -zm2[j].y);
         }
-        const float4 s4 = *reinterpret_cast<const float4*>(st + kWTileBytes + rg * 16);
-        const float4 r4 = *reinterpret_cast<const float4*>(st + kWTileBytes + kSBytes + rg * 16);
-        const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
-        const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
-        uint32_t o[4][4];
+        const uint8_t* wrow = st + h * (kWTileBytes / 2) + (rg * 8) * 128 + c8 * 16;
+        const float* srow = reinterpret_cast<const float*>(st + kWTileBytes) + rg * 8;
+        const float* rrow = reinterpret_cast<const float*>(st + kWTileBytes + kSBytes) + rg * 8;
+        uint8_t* brow = smem + kOffB + s * kBBytes + h * (kBK * 128) + (rg * 8) * 128;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = rg * 4 + i;
-          const uint4 wv = *reinterpret_cast<const uint4*>(st + h * (kWTileBytes / 2) + row * 128 + c8 * 16);
-          const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
-          const float2 s2 = make_float2(sv[i], sv[i]);
-          const float2 r2 = make_float2(rv[i], rv[i]);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[4][4];
+          produce4(wrow + half * 4 * 128, *reinterpret_cast<const float4*>(srow + half * 4),
+                   *reinterpret_cast<const float4*>(rrow + half * 4), inv2, zm2, nzm2, nstep2, lo, hi, o);
+          // the operand slot is reused once the MMAs that read it 3 steps ago completed
+          if (half == 0 && it >= kStages &&
+              !mbar_wait_cluster(&empty_bar[s], ((it / kStages) & 1) ^ 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // w' = w s;  t = rint(w'/step) + zero (held as 1.5*2^23 + code);
-            // clamp to the code range; the negated difference
-            // (w' - (code - zero) step) / s = W - S^-1 W'hat (its squares
-            // give the same loss)
-            const float2 w2 = make_float2(bf16lo(wu[j]), bf16hi(wu[j]));
-            const float2 wp = __fmul2_rn(w2, s2);
-            float2 tq = __ffma2_rn(wp, inv2[j], zm2[j]);
-            tq.x = fminf(fmaxf(tq.x, lo), hi);
-            tq.y = fminf(fmaxf(tq.y, lo), hi);
-            const float2 qz = __fadd2_rn(tq, nzm2[j]);
-            const float2 ev = __ffma2_rn(qz, nstep2[j], wp);
-            const float2 d = __fmul2_rn(ev, r2);
-            o[i][j] = pack_bf16x2(d.x, d.y);
+          for (int i = 0; i < 4; ++i) {
+            const int r = half * 4 + i;  // row within the thread's 8 (row & 7 == r)
+            *reinterpret_cast<uint4*>(brow + r * 128 + ((c8 ^ r) * 16)) = make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
           }
         }
-        // every input of this stage is in registers: free it for the loader
+        if (!ok) break;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&wempty_bar[ws]);
-        // the operand slot is reused once the MMAs that read it 3 steps ago completed
-        if (it >= kStages && !mbar_wait_cluster(&empty_bar[s], ((it / kStages) & 1) ^ 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        uint8_t* bst = smem + kOffB + s * kBBytes + h * (kBK * 128);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = rg * 4 + i;
-          *reinterpret_cast<uint4*>(bst + row * 128 + ((c8 ^ (row & 7)) * 16)) =
-              make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
-        }
-        fence_proxy_async_smem();
+        if (lane == 0) mbar_arrive(&wempty_bar[ws]);  // the loader may refill this input stage
+        fence_proxy_async_smem();                     // stores visible to the tensor cores
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(full_mine + static_cast<uint32_t>(s) * 8u);
+        if (lane == 0) mbar_arrive_remote(full0 + static_cast<uint32_t>(s) * 8u);
       }
       if (!ok) break;
     }

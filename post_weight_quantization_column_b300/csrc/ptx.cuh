@@ -190,9 +190,15 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-// Arrive (release, cluster scope) on an mbarrier given by a shared::cluster address.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// Arrive on an mbarrier given by a shared::cluster address (possibly in the
+// peer CTA), with the instruction's default CTA-scope release.  A
+// cluster-scope release costs about 1.4k cycles here (it drains the thread's
+// memory operations to cluster scope); the data these arrivals publish is
+// either already in registers (TMEM reads completed by tcgen05.wait::ld) or
+// shared-memory stores ordered for the tensor cores by fence.proxy.async
+// before the arrive.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
