@@ -19,7 +19,7 @@ using namespace awqdev;
 
 namespace {
 
-constexpr size_t kHeaderBytes = 256;  // status word lives at offset 0
+constexpr size_t kHeaderBytes = 256;  // status word at offset 0, reduction ticket at offset 4
 constexpr int kMaxDevices = 64;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -154,7 +154,7 @@ size_t stats_ws_bytes(int64_t N, int64_t D_in) {
 }
 
 struct SearchLayout {
-  size_t s_tab, r_tab, qp, partial, col, dW, total;
+  size_t s_tab, r_tab, qp, partial, col, blk, dW, total;
   int m_tiles;
 };
 
@@ -175,6 +175,8 @@ SearchLayout search_layout(int64_t N, int64_t D_in, int64_t D_out, int G, int gr
   off = align_up(off + g * static_cast<size_t>(L.m_tiles) * dout * 4, 256);
   L.col = off;
   off = align_up(off + g * dout * 8, 256);
+  L.blk = off;
+  off = align_up(off + g * static_cast<size_t>(reduce_blocks(D_out)) * 8, 256);
   L.dW = off;
   if (mat) off = align_up(off + g * din * dout * 2, 256);
   L.total = off;
@@ -300,7 +302,8 @@ awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int
   double* col = col_losses ? col_losses : reinterpret_cast<double*>(base + L.col);
   void* dW = base + L.dW;
 
-  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return AWQ_ERR_CUDA;
+  // status word and the reduction's ticket counter
+  if (cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return AWQ_ERR_CUDA;
   cudaError_t e;
   {
     ProfScope prof("scale_table", s);
@@ -326,7 +329,9 @@ awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int
   }
   if (e == cudaSuccess) {
     ProfScope prof("reduce_argmin", s);
-    e = launch_reduce_losses(partial, L.m_tiles, D_out, G, col, losses, best_idx, s_tab, D_in, s_star, status, s);
+    e = launch_reduce_losses(partial, L.m_tiles, D_out, G, col, reinterpret_cast<double*>(base + L.blk),
+                             reinterpret_cast<unsigned int*>(base + 4), losses, best_idx, s_tab, D_in, s_star, status,
+                             s);
   }
   return from_cuda(e);
 }

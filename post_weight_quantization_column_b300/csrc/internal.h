@@ -14,7 +14,7 @@ namespace awqdev {
 constexpr int kStatsThreads = 256;
 constexpr int kStatsRowLanes = 8;      // warps per CTA, each on its own rows
 constexpr int kStatsCols = 256;        // channels per CTA (32 lanes x 8)
-constexpr int kStatsTargetCtas = 148 * 8;
+constexpr int kStatsTargetCtas = 148 * 2;
 constexpr int kStatsMaxSplits = 1024;
 
 void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split);
@@ -76,8 +76,11 @@ cudaError_t launch_search_fused(PFN_cuTensorMapEncodeTiled_v12000 encode, const 
                                 uint32_t* status, int max_pairs, cudaStream_t stream);
 
 // ----------------------------------------------------------------- reductions
+int reduce_blocks(int64_t D_out);
+// blk: fp64 [G][reduce_blocks(D_out)] scratch; ticket: a zeroed uint32 (left zeroed).
 cudaError_t launch_reduce_losses(const float* partial, int m_tiles, int64_t D_out, int G, double* col_losses,
-                                 double* losses, int32_t* best_idx, const float* s_tab, int64_t D_in, float* s_star,
-                                 uint32_t* status, cudaStream_t stream);
+                                 double* blk, unsigned int* ticket, double* losses, int32_t* best_idx,
+                                 const float* s_tab, int64_t D_in, float* s_star, uint32_t* status,
+                                 cudaStream_t stream);
 
 }  // namespace awqdev

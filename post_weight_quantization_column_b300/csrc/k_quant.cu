@@ -77,108 +77,169 @@ __device__ __forceinline__ QParam make_qparam(float lo, float hi, int symmetric,
   return q;
 }
 
-// One CTA: one group of GS rows x 256 columns, all G candidates.  The W tile
-// and the group's slice of the scale table sit in shared memory; each thread
-// owns two adjacent columns and scans the group once per candidate.
+// Running min / max of three values (sm_100 three-input forms; exact, so the
+// order of the comparisons does not matter).
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// max(|a|, |b|, |c|)
+__device__ __forceinline__ float fmaxabs3(float a, float b, float c) {
+  float d;
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+constexpr int kGpThreads = 128;   // one output column per thread
+constexpr int kGpCols = kGpThreads;
+constexpr int kMaxGpCandidates = 32;  // candidates per CTA (grid.z splits larger grids)
+
+// One CTA: one group of GS rows x 128 columns, up to 32 candidates.  The W tile
+// (GS x 128 bf16) and the group's scale rows sit in shared memory, the
+// scales as {s_k[r], s_k[r+1]} pairs so that one 8-byte broadcast load feeds
+// a packed multiply.  Thread t owns column t and keeps the running range of
+// all G candidates in registers: for each pair of rows it unpacks its two
+// weights once, then per candidate does w' = w s for both rows in one packed
+// multiply and a three-input min / max against the running range.
 template <int GS>
-__global__ void __launch_bounds__(128) group_params_kernel(const __nv_bfloat16* __restrict__ W,
-                                                         const float* __restrict__ s_tab, int64_t D_in,
-                                                         int64_t D_out, int G, int symmetric,
-                                                         float* __restrict__ qp, uint32_t* status) {
+__global__ void __launch_bounds__(kGpThreads) group_params_kernel(const __nv_bfloat16* __restrict__ W,
+                                                                const float* __restrict__ s_tab, int64_t D_in,
+                                                                int64_t D_out, int G, int symmetric,
+                                                                float* __restrict__ qp, uint32_t* status) {
   extern __shared__ __align__(16) uint8_t smem[];
-  uint32_t* wsh = reinterpret_cast<uint32_t*>(smem);             // [GS][128] bf16 pairs
-  float* ssh = reinterpret_cast<float*>(smem + GS * 128 * 4);    // [G][GS]
+  __nv_bfloat16* wsh = reinterpret_cast<__nv_bfloat16*>(smem);     // [GS][128]
+  float2* ssh = reinterpret_cast<float2*>(smem + GS * kGpCols * 2);  // [GS/2][nk]
   const int t = threadIdx.x;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 256;
+  const int k0 = blockIdx.z * kMaxGpCandidates;
+  const int nk = min(kMaxGpCandidates, G - k0);
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kGpCols;
   const int64_t grp = blockIdx.y;
   const int64_t j0 = grp * GS;
   bool bad = false;
-  for (int idx = t; idx < GS * 32; idx += 128) {
-    const int r = idx >> 5;
-    const int c8 = idx & 31;
-    const int64_t col = n0 + c8 * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (col < D_out) v = *reinterpret_cast<const uint4*>(W + (j0 + r) * D_out + col);
-    bad |= bf16x2_nonfinite(v.x) | bf16x2_nonfinite(v.y) | bf16x2_nonfinite(v.z) | bf16x2_nonfinite(v.w);
-    *reinterpret_cast<uint4*>(&wsh[r * 128 + c8 * 4]) = v;
+  {
+    // all of the thread's loads in flight before the first store
+    constexpr int kLoads = GS * (kGpCols / 8) / kGpThreads;
+    uint4 v[kLoads];
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) {
+      const int idx = t + i * kGpThreads;
+      const int64_t col = n0 + (idx & 15) * 8;
+      v[i] = col < D_out ? *reinterpret_cast<const uint4*>(W + (j0 + (idx >> 4)) * D_out + col)
+                         : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) {
+      const int idx = t + i * kGpThreads;
+      bad |= bf16x2_nonfinite(v[i].x) | bf16x2_nonfinite(v[i].y) | bf16x2_nonfinite(v[i].z) |
+             bf16x2_nonfinite(v[i].w);
+      *reinterpret_cast<uint4*>(wsh + (idx >> 4) * kGpCols + (idx & 15) * 8) = v[i];
+    }
   }
-  for (int idx = t; idx < G * GS; idx += 128) {
-    const int k = idx / GS;
-    const int r = idx - k * GS;
-    ssh[idx] = s_tab[static_cast<int64_t>(k) * D_in + j0 + r];
+  {
+    // scale pairs, up to kMaxGpCandidates * GS/2 of them: all loads first
+    constexpr int kSLoads = kMaxGpCandidates * (GS / 2) / kGpThreads;
+    float2 sv[kSLoads];
+#pragma unroll
+    for (int i = 0; i < kSLoads; ++i) {
+      const int idx = t + i * kGpThreads;
+      const int k = idx / (GS / 2);
+      const int rp = idx - k * (GS / 2);
+      sv[i] = k < nk ? *reinterpret_cast<const float2*>(s_tab + static_cast<int64_t>(k0 + k) * D_in + j0 + 2 * rp)
+                     : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kSLoads; ++i) {
+      const int idx = t + i * kGpThreads;
+      const int k = idx / (GS / 2);
+      const int rp = idx - k * (GS / 2);
+      if (k < nk) ssh[rp * nk + k] = sv[i];
+    }
   }
-  if (bad) set_error(status, AWQ_DEV_NONFINITE);
+  if (bad && blockIdx.z == 0) set_error(status, AWQ_DEV_NONFINITE);
   __syncthreads();
-  const int64_t n = n0 + 2 * t;
-  const int64_t T = D_in / GS;
-  for (int k = 0; k < G; ++k) {
-    const float* sk = ssh + k * GS;
-    float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;
+  const int64_t n = n0 + t;
+  if (n >= D_out) return;
+
+  float lo[kMaxGpCandidates], hi[kMaxGpCandidates];
+#pragma unroll
+  for (int k = 0; k < kMaxGpCandidates; ++k) lo[k] = hi[k] = 0.f;
+  const uint16_t* wcol = reinterpret_cast<const uint16_t*>(wsh) + t;
+#pragma unroll 2
+  for (int rp = 0; rp < GS / 2; ++rp) {
+    const float2 w2 = make_float2(__uint_as_float(static_cast<uint32_t>(wcol[(2 * rp) * kGpCols]) << 16),
+                                  __uint_as_float(static_cast<uint32_t>(wcol[(2 * rp + 1) * kGpCols]) << 16));
+    const float2* sp = ssh + rp * nk;
     if (symmetric) {
-#pragma unroll 8
-      for (int r = 0; r < GS; ++r) {
-        const uint32_t u = wsh[r * 128 + t];
-        const float s = sk[r];
-        hi0 = fmaxf(hi0, fabsf(__fmul_rn(bf16lo(u), s)));
-        hi1 = fmaxf(hi1, fabsf(__fmul_rn(bf16hi(u), s)));
+#pragma unroll
+      for (int k = 0; k < kMaxGpCandidates; ++k) {
+        if (k < nk) {
+          const float2 p = __fmul2_rn(w2, sp[k]);
+          hi[k] = fmaxabs3(hi[k], p.x, p.y);
+        }
       }
     } else {
-#pragma unroll 8
-      for (int r = 0; r < GS; ++r) {
-        const uint32_t u = wsh[r * 128 + t];
-        const float s = sk[r];
-        const float p0 = __fmul_rn(bf16lo(u), s);
-        const float p1 = __fmul_rn(bf16hi(u), s);
-        lo0 = fminf(lo0, p0);
-        hi0 = fmaxf(hi0, p0);
-        lo1 = fminf(lo1, p1);
-        hi1 = fmaxf(hi1, p1);
+#pragma unroll
+      for (int k = 0; k < kMaxGpCandidates; ++k) {
+        if (k < nk) {
+          const float2 p = __fmul2_rn(w2, sp[k]);
+          lo[k] = fmin3(lo[k], p.x, p.y);
+          hi[k] = fmax3(hi[k], p.x, p.y);
+        }
       }
     }
-    if (n < D_out) {
-      // n is even, so both columns sit in one 8-column chunk
-      float* dst = qp + ((static_cast<int64_t>(k) * T + grp) * (D_out / kQChunkCols) + n / kQChunkCols) * kQChunkFloats +
-                   (n % kQChunkCols);
-      const QParam q0 = make_qparam(lo0, hi0, symmetric, status);
-      const QParam q1 = make_qparam(lo1, hi1, symmetric, status);
-      dst[0] = q0.inv;
-      dst[1] = q1.inv;
-      dst[kQChunkCols] = q0.zm;
-      dst[kQChunkCols + 1] = q1.zm;
-      dst[2 * kQChunkCols] = q0.step;
-      dst[2 * kQChunkCols + 1] = q1.step;
+  }
+  const int64_t T = D_in / GS;
+  const int64_t kstride = T * (D_out / kQChunkCols) * kQChunkFloats;
+  float* dst0 = qp + k0 * kstride + (grp * (D_out / kQChunkCols) + n / kQChunkCols) * kQChunkFloats +
+                (n % kQChunkCols);
+#pragma unroll
+  for (int k = 0; k < kMaxGpCandidates; ++k) {
+    if (k < nk) {
+      const QParam q = make_qparam(lo[k], hi[k], symmetric, status);
+      float* dst = dst0 + k * kstride;
+      dst[0] = q.inv;
+      dst[kQChunkCols] = q.zm;
+      dst[2 * kQChunkCols] = q.step;
     }
   }
 }
 
-static size_t group_params_smem(int GS, int G) { return static_cast<size_t>(GS) * 512 + static_cast<size_t>(G) * GS * 4; }
+static size_t group_params_smem(int GS) {
+  return static_cast<size_t>(GS) * kGpCols * 2 + static_cast<size_t>(GS / 2) * kMaxGpCandidates * 8;
+}
+
+template <int GS>
+static cudaError_t launch_group_params_t(const __nv_bfloat16* W, const float* s_tab, int64_t D_in, int64_t D_out,
+                                         int G, int symmetric, float* qp, uint32_t* status, cudaStream_t stream) {
+  const size_t smem = group_params_smem(GS);
+  cudaError_t e = cudaFuncSetAttribute(group_params_kernel<GS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>((D_out + kGpCols - 1) / kGpCols), static_cast<unsigned>(D_in / GS),
+                  static_cast<unsigned>((G + kMaxGpCandidates - 1) / kMaxGpCandidates));
+  group_params_kernel<GS><<<grid, kGpThreads, smem, stream>>>(W, s_tab, D_in, D_out, G, symmetric, qp, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in, int64_t D_out, int G,
                                 int group_size, int symmetric, float* qp, uint32_t* status, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>((D_out + 255) / 256), static_cast<unsigned>(D_in / group_size));
-  const size_t smem = group_params_smem(group_size, G);
   const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
-  cudaError_t e;
   switch (group_size) {
     case 64:
-      e = cudaFuncSetAttribute(group_params_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      group_params_kernel<64><<<grid, 128, smem, stream>>>(Wb, s_tab, D_in, D_out, G, symmetric, qp, status);
-      break;
+      return launch_group_params_t<64>(Wb, s_tab, D_in, D_out, G, symmetric, qp, status, stream);
     case 128:
-      e = cudaFuncSetAttribute(group_params_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      group_params_kernel<128><<<grid, 128, smem, stream>>>(Wb, s_tab, D_in, D_out, G, symmetric, qp, status);
-      break;
+      return launch_group_params_t<128>(Wb, s_tab, D_in, D_out, G, symmetric, qp, status, stream);
     case 256:
-      e = cudaFuncSetAttribute(group_params_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      group_params_kernel<256><<<grid, 128, smem, stream>>>(Wb, s_tab, D_in, D_out, G, symmetric, qp, status);
-      break;
+      return launch_group_params_t<256>(Wb, s_tab, D_in, D_out, G, symmetric, qp, status, stream);
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ candidate materialisation
@@ -251,10 +312,12 @@ cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r
 // W_quantized = Quantize(diag(s*) W); "009. AWQ Integration", Consequences:
 // two 4-bit codes per byte (even input row in the low nibble).
 //
-// One CTA: one group (GS rows) x 256 columns.  Lane l of warp w owns columns
-// [8l, 8l+8) and rows [w*RPT, (w+1)*RPT), RPT = GS/8, held in registers as
-// bf16 pairs.  Pass 1 finds the per-column range (fixed-order combine of the
-// 8 warps in shared memory) and the exact step / zero; pass 2 emits codes.
+// One CTA: one group (GS rows) x 64 columns, 256 threads.  Thread t owns the
+// 8 columns of chunk c = t % 8 and the row pairs (2p + 64i, 2p + 64i + 1),
+// p = t / 8, i < GS/64, so that both rows of a packed byte sit in one
+// thread.  Pass 1 finds the per-column range (shuffles over the 4 row slots
+// of a warp, then the 8 warps in a fixed order in shared memory) and the
+// exact step / zero; pass 2 emits codes.
 //
 // Codes equal clamp(rint(fp32(w'/step)) + zero): the quotient is first
 // formed as w' * (1/step); where that lands within 8e-6 of a half-integer
@@ -262,65 +325,82 @@ cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r
 // the IEEE division.  |w'/step| <= 45 in every case, where the product is
 // within 6e-6 of the IEEE quotient, so elsewhere both round alike.
 constexpr float kTieGuard = 0.5f - 8.0e-6f;
+constexpr int kPackCols = 64;
 
-template <int RPT>
+template <int GS>
 __global__ void __launch_bounds__(256) pack_kernel(const __nv_bfloat16* __restrict__ W, const float* __restrict__ s,
                                                  int64_t D_in, int64_t D_out, int symmetric,
                                                  uint8_t* __restrict__ qweight, __half* __restrict__ scales,
                                                  __half* __restrict__ zeros, uint32_t* status) {
-  constexpr int GS = RPT * 8;
-  __shared__ float red_lo[8][256];
-  __shared__ float red_hi[8][256];
-  __shared__ float4 prm[256];   // {step, 1/step, zoff, zero}
-  const int lane = threadIdx.x & 31;
-  const int wp_ = threadIdx.x >> 5;
-  const int64_t n = static_cast<int64_t>(blockIdx.x) * 256 + lane * 8;
+  constexpr int NP = GS / 64;  // row pairs per thread
+  constexpr int NR = 2 * NP;   // rows per thread
+  __shared__ float red_lo[8][kPackCols];
+  __shared__ float red_hi[8][kPackCols];
+  __shared__ float4 prm[kPackCols];  // {step, 1/step, zoff, zero}
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int wp_ = t >> 5;
+  const int c = t & 7;
+  const int pslot = t >> 3;
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * kPackCols + c * 8;
   const int64_t grp = blockIdx.y;
-  const int64_t j0 = grp * GS + wp_ * RPT;
+  const int64_t jb = grp * GS + 2 * pslot;  // row pair i: jb + 64 i, jb + 64 i + 1
   const bool active = n < D_out;
 
-  uint4 w[RPT];
-  float sj[RPT];
+  uint4 w[NR];
+  float sj[NR];
   bool bad = false;
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    sj[i] = s[j0 + i];
-    w[i] = active ? *reinterpret_cast<const uint4*>(W + (j0 + i) * D_out + n) : make_uint4(0u, 0u, 0u, 0u);
-    bad |= bf16x2_nonfinite(w[i].x) | bf16x2_nonfinite(w[i].y) | bf16x2_nonfinite(w[i].z) |
-           bf16x2_nonfinite(w[i].w);
+  for (int i = 0; i < NR; ++i) {
+    const int64_t row = jb + 64 * (i >> 1) + (i & 1);
+    sj[i] = s[row];
+    w[i] = active ? *reinterpret_cast<const uint4*>(W + row * D_out + n) : make_uint4(0u, 0u, 0u, 0u);
+    bad |= bf16x2_nonfinite(w[i].x) | bf16x2_nonfinite(w[i].y) | bf16x2_nonfinite(w[i].z) | bf16x2_nonfinite(w[i].w);
   }
   if (bad) set_error(status, AWQ_DEV_NONFINITE);
 
-  // pass 1: per-column range of w' = w * s over this thread's rows
+  // pass 1: per-column range of w' = w * s over this thread's rows (two rows
+  // per step: packed products, three-input min / max)
   float lo[8], hi[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) lo[c] = hi[c] = 0.f;
+  for (int k = 0; k < 8; ++k) lo[k] = hi[k] = 0.f;
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    const uint32_t wu[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+  for (int i = 0; i < NR; i += 2) {
+    const uint32_t we[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+    const uint32_t wo[4] = {w[i + 1].x, w[i + 1].y, w[i + 1].z, w[i + 1].w};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float p0 = __fmul_rn(bf16lo(wu[c]), sj[i]);
-      const float p1 = __fmul_rn(bf16hi(wu[c]), sj[i]);
+    for (int k = 0; k < 4; ++k) {
+      const float2 pe = __fmul2_rn(make_float2(bf16lo(we[k]), bf16hi(we[k])), make_float2(sj[i], sj[i]));
+      const float2 po = __fmul2_rn(make_float2(bf16lo(wo[k]), bf16hi(wo[k])), make_float2(sj[i + 1], sj[i + 1]));
       if (symmetric) {
-        hi[2 * c] = fmaxf(hi[2 * c], fabsf(p0));
-        hi[2 * c + 1] = fmaxf(hi[2 * c + 1], fabsf(p1));
+        hi[2 * k] = fmaxabs3(hi[2 * k], pe.x, po.x);
+        hi[2 * k + 1] = fmaxabs3(hi[2 * k + 1], pe.y, po.y);
       } else {
-        lo[2 * c] = fminf(lo[2 * c], p0);
-        hi[2 * c] = fmaxf(hi[2 * c], p0);
-        lo[2 * c + 1] = fminf(lo[2 * c + 1], p1);
-        hi[2 * c + 1] = fmaxf(hi[2 * c + 1], p1);
+        lo[2 * k] = fmin3(lo[2 * k], pe.x, po.x);
+        hi[2 * k] = fmax3(hi[2 * k], pe.x, po.x);
+        lo[2 * k + 1] = fmin3(lo[2 * k + 1], pe.y, po.y);
+        hi[2 * k + 1] = fmax3(hi[2 * k + 1], pe.y, po.y);
       }
     }
   }
+  // lanes l, l^8, l^16, l^24 hold the same columns (four row slots)
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    red_lo[wp_][lane * 8 + c] = lo[c];
-    red_hi[wp_][lane * 8 + c] = hi[c];
+  for (int k = 0; k < 8; ++k) {
+    lo[k] = fminf(lo[k], __shfl_xor_sync(0xFFFFFFFFu, lo[k], 8));
+    hi[k] = fmaxf(hi[k], __shfl_xor_sync(0xFFFFFFFFu, hi[k], 8));
+    lo[k] = fminf(lo[k], __shfl_xor_sync(0xFFFFFFFFu, lo[k], 16));
+    hi[k] = fmaxf(hi[k], __shfl_xor_sync(0xFFFFFFFFu, hi[k], 16));
+  }
+  if (lane < 8) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      red_lo[wp_][c * 8 + k] = lo[k];
+      red_hi[wp_][c * 8 + k] = hi[k];
+    }
   }
   __syncthreads();
-  {
-    const int col = threadIdx.x;
+  if (t < kPackCols) {
+    const int col = t;
     float l = 0.f, h = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -338,7 +418,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __nv_bfloat16* __restri
       z = static_cast<float>(static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(-l, sc)), 0.f), 15.f)));
     const float zoff = symmetric ? 8.f : z;
     prm[col] = make_float4(sc, sc != 0.f ? __frcp_rn(sc) : 0.f, zoff, symmetric ? 8.f : z);
-    const int64_t ncol = static_cast<int64_t>(blockIdx.x) * 256 + col;
+    const int64_t ncol = static_cast<int64_t>(blockIdx.x) * kPackCols + col;
     if (ncol < D_out) {
       scales[grp * D_out + ncol] = __float2half_rn(sc);
       zeros[grp * D_out + ncol] = __float2half_rn(symmetric ? 8.f : z);
@@ -349,89 +429,98 @@ __global__ void __launch_bounds__(256) pack_kernel(const __nv_bfloat16* __restri
 
   float step[8], inv[8], zmz[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const float4 p = prm[lane * 8 + c];
-    step[c] = p.x;
-    inv[c] = p.y;
-    zmz[c] = kMagic + p.z;
+  for (int k = 0; k < 8; ++k) {
+    const float4 pr = prm[c * 8 + k];
+    step[k] = pr.x;
+    inv[k] = pr.y;
+    zmz[k] = kMagic + pr.z;
   }
   const float clo = symmetric ? kMagic + 1.f : kMagic;
   const float chi = kMagic + 15.f;
 
-  // pass 2 (fast): codes through the reciprocal, with a near-tie flag
-  uint32_t out[RPT / 2][2];
-  bool tie = false;
+  // pass 2 (fast): codes through the reciprocal.  y = w' (1/step); c =
+  // y + 1.5*2^23 + zero rounds it to an integer; tmax tracks the largest
+  // |y - rint(y)|, which flags a near tie anywhere in the thread's elements.
+  uint32_t out[NP][2];
+  float tmax = 0.f;
 #pragma unroll
-  for (int i = 0; i < RPT; i += 2) {
-    const uint32_t we[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-    const uint32_t wo[4] = {w[i + 1].x, w[i + 1].y, w[i + 1].z, w[i + 1].w};
+  for (int i = 0; i < NP; ++i) {
+    const uint32_t we[4] = {w[2 * i].x, w[2 * i].y, w[2 * i].z, w[2 * i].w};
+    const uint32_t wo[4] = {w[2 * i + 1].x, w[2 * i + 1].y, w[2 * i + 1].z, w[2 * i + 1].w};
     uint32_t bytes[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float xe = (c & 1) ? bf16hi(we[c >> 1]) : bf16lo(we[c >> 1]);
-      const float xo = (c & 1) ? bf16hi(wo[c >> 1]) : bf16lo(wo[c >> 1]);
-      const float ye = __fmul_rn(__fmul_rn(xe, sj[i]), inv[c]);
-      const float yo = __fmul_rn(__fmul_rn(xo, sj[i + 1]), inv[c]);
-      float ce = __fadd_rn(ye, zmz[c]);
-      float co = __fadd_rn(yo, zmz[c]);
-      tie |= fabsf(__fsub_rn(ye, __fsub_rn(ce, zmz[c]))) > kTieGuard;
-      tie |= fabsf(__fsub_rn(yo, __fsub_rn(co, zmz[c]))) > kTieGuard;
-      ce = fminf(fmaxf(ce, clo), chi);
-      co = fminf(fmaxf(co, clo), chi);
-      bytes[c] = (__float_as_uint(ce) & 0xFu) | ((__float_as_uint(co) & 0xFu) << 4);
+    for (int k = 0; k < 4; ++k) {
+      const float2 inv2 = make_float2(inv[2 * k], inv[2 * k + 1]);
+      const float2 zm2 = make_float2(zmz[2 * k], zmz[2 * k + 1]);
+      const float2 nzm2 = make_float2(-zmz[2 * k], -zmz[2 * k + 1]);
+      const float2 ye = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(we[k]), bf16hi(we[k])), make_float2(sj[2 * i], sj[2 * i])), inv2);
+      const float2 yo = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(wo[k]), bf16hi(wo[k])), make_float2(sj[2 * i + 1], sj[2 * i + 1])), inv2);
+      float2 ce = __fadd2_rn(ye, zm2);
+      float2 co = __fadd2_rn(yo, zm2);
+      const float2 de = __ffma2_rn(ye, make_float2(-1.f, -1.f), __fadd2_rn(ce, nzm2));
+      const float2 dd = __ffma2_rn(yo, make_float2(-1.f, -1.f), __fadd2_rn(co, nzm2));
+      tmax = fmaxabs3(tmax, de.x, de.y);
+      tmax = fmaxabs3(tmax, dd.x, dd.y);
+      ce.x = fminf(fmaxf(ce.x, clo), chi);
+      ce.y = fminf(fmaxf(ce.y, clo), chi);
+      co.x = fminf(fmaxf(co.x, clo), chi);
+      co.y = fminf(fmaxf(co.y, clo), chi);
+      bytes[2 * k] = (__float_as_uint(ce.x) & 0xFu) | ((__float_as_uint(co.x) & 0xFu) << 4);
+      bytes[2 * k + 1] = (__float_as_uint(ce.y) & 0xFu) | ((__float_as_uint(co.y) & 0xFu) << 4);
     }
-    out[i / 2][0] = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
-    out[i / 2][1] = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+    out[i][0] = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+    out[i][1] = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
   }
+  const bool tie = tmax > kTieGuard;
   if (tie) {
     // slow path: IEEE quotient for every element of this thread
 #pragma unroll
-    for (int i = 0; i < RPT; i += 2) {
-      const uint32_t we[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-      const uint32_t wo[4] = {w[i + 1].x, w[i + 1].y, w[i + 1].z, w[i + 1].w};
+    for (int i = 0; i < NP; ++i) {
+      const uint32_t we[4] = {w[2 * i].x, w[2 * i].y, w[2 * i].z, w[2 * i].w};
+      const uint32_t wo[4] = {w[2 * i + 1].x, w[2 * i + 1].y, w[2 * i + 1].z, w[2 * i + 1].w};
       uint32_t bytes[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float xe = (c & 1) ? bf16hi(we[c >> 1]) : bf16lo(we[c >> 1]);
-        const float xo = (c & 1) ? bf16hi(wo[c >> 1]) : bf16lo(wo[c >> 1]);
+      for (int k = 0; k < 8; ++k) {
+        const float xe = (k & 1) ? bf16hi(we[k >> 1]) : bf16lo(we[k >> 1]);
+        const float xo = (k & 1) ? bf16hi(wo[k >> 1]) : bf16lo(wo[k >> 1]);
         // clamp(rint(IEEE w'/step) + zoff, clo, 15); a zero step keeps code zoff
-        uint32_t ke = static_cast<uint32_t>(zmz[c] - kMagic), ko = ke;
-        if (step[c] != 0.f) {
-          const float zo = zmz[c] - kMagic;
+        uint32_t ke = static_cast<uint32_t>(zmz[k] - kMagic), ko = ke;
+        if (step[k] != 0.f) {
+          const float zo = zmz[k] - kMagic;
           const float ql = clo - kMagic;
-          const float qe = rintf(__fdiv_rn(__fmul_rn(xe, sj[i]), step[c])) + zo;
-          const float qo = rintf(__fdiv_rn(__fmul_rn(xo, sj[i + 1]), step[c])) + zo;
+          const float qe = rintf(__fdiv_rn(__fmul_rn(xe, sj[2 * i]), step[k])) + zo;
+          const float qo = rintf(__fdiv_rn(__fmul_rn(xo, sj[2 * i + 1]), step[k])) + zo;
           ke = static_cast<uint32_t>(fminf(fmaxf(qe, ql), 15.f));
           ko = static_cast<uint32_t>(fminf(fmaxf(qo, ql), 15.f));
         }
-        bytes[c] = ke | (ko << 4);
+        bytes[k] = ke | (ko << 4);
       }
-      out[i / 2][0] = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
-      out[i / 2][1] = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+      out[i][0] = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+      out[i][1] = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
     }
   }
 #pragma unroll
-  for (int i = 0; i < RPT; i += 2) {
-    const int64_t row = (j0 + i) / 2;
-    *reinterpret_cast<uint2*>(qweight + row * D_out + n) = make_uint2(out[i / 2][0], out[i / 2][1]);
+  for (int i = 0; i < NP; ++i) {
+    const int64_t prow = (jb + 64 * i) / 2;
+    *reinterpret_cast<uint2*>(qweight + prow * D_out + n) = make_uint2(out[i][0], out[i][1]);
   }
 }
 
 cudaError_t launch_pack(const void* W, const float* s, int64_t D_in, int64_t D_out, int group_size, int symmetric,
                         uint8_t* qweight, void* scales, void* zeros, uint32_t* status, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>((D_out + 255) / 256), static_cast<unsigned>(D_in / group_size));
+  const dim3 grid(static_cast<unsigned>((D_out + kPackCols - 1) / kPackCols), static_cast<unsigned>(D_in / group_size));
   const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
   __half* sc = static_cast<__half*>(scales);
   __half* zr = static_cast<__half*>(zeros);
   switch (group_size) {
     case 64:
-      pack_kernel<8><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
+      pack_kernel<64><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
       break;
     case 128:
-      pack_kernel<16><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
+      pack_kernel<128><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
       break;
     case 256:
-      pack_kernel<32><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
+      pack_kernel<256><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
       break;
     default:
       return cudaErrorInvalidValue;

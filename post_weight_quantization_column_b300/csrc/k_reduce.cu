@@ -1,6 +1,6 @@
 // Loss reduction and argmin ("AWQ (Activation-aware Weight Quantization)",
-// 缩放因子优化的完整流程 steps 4c-6): the GEMM leaves one fp32 sum of squares
-// per (candidate, 128-row tile, column); these are summed in fp64 in a fixed
+// 缩放因子优化的完整流程 steps 4c-6): the search leaves one fp32 sum of squares
+// per (candidate, row tile, column); these are summed in fp64 in a fixed
 // order, first over row tiles (per-column losses), then over columns (L_k),
 // then k* = first argmin and s* = s_k* is copied out.
 #include "internal.h"
@@ -8,47 +8,71 @@
 
 namespace awqdev {
 
-__global__ void reduce_rows_kernel(const float* __restrict__ partial, int m_tiles, int64_t D_out,
-                                   double* __restrict__ col) {
-  const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int k = blockIdx.y;
-  if (n >= D_out) return;
-  const float* p = partial + static_cast<int64_t>(k) * m_tiles * D_out + n;
-  double s = 0.0;
-  for (int m = 0; m < m_tiles; ++m) s += static_cast<double>(p[static_cast<int64_t>(m) * D_out]);
-  col[static_cast<int64_t>(k) * D_out + n] = s;
-}
-
 constexpr int kRedThreads = 256;
 
-__global__ void __launch_bounds__(kRedThreads) reduce_cols_kernel(const double* __restrict__ col, int64_t D_out,
-                                                                 double* __restrict__ losses) {
+// One kernel for the whole reduction.  CTA (bx, k) owns columns
+// [256 bx, 256 bx + 256) of candidate k: each thread sums its column over the
+// row tiles (fp64, tile order) into col[k][n]; the CTA then sums its 256
+// columns in a fixed tree into blk[k][bx].  The last CTA to finish (a ticket
+// counter that the caller zeroed) adds blk[k][0..nb) in block order into
+// L_k, picks k* = first argmin and copies s* = s_k*.  Every sum has a fixed
+// order, so the result does not depend on timing.
+__global__ void __launch_bounds__(kRedThreads)
+    reduce_losses_kernel(const float* __restrict__ partial, int m_tiles, int64_t D_out, int G,
+                         double* __restrict__ col, double* __restrict__ blk, unsigned int* __restrict__ ticket,
+                         double* __restrict__ losses, int32_t* __restrict__ best_idx, const float* __restrict__ s_tab,
+                         int64_t D_in, float* __restrict__ s_star, uint32_t* status) {
   __shared__ double sh[kRedThreads];
-  const int k = blockIdx.x;
-  const double* c = col + static_cast<int64_t>(k) * D_out;
-  double s = 0.0;
-  for (int64_t n = threadIdx.x; n < D_out; n += kRedThreads) s += c[n];
-  sh[threadIdx.x] = s;
+  __shared__ bool last;
+  __shared__ int kbest;
+  const int k = blockIdx.y;
+  const int nb = gridDim.x;
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * kRedThreads + threadIdx.x;
+  double v = 0.0;
+  if (n < D_out) {
+    const float* p = partial + static_cast<int64_t>(k) * m_tiles * D_out + n;
+    int m = 0;
+    for (; m + 8 <= m_tiles; m += 8) {
+      float x[8];  // eight loads in flight, added in tile order
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = p[static_cast<int64_t>(m + i) * D_out];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v += static_cast<double>(x[i]);
+    }
+    for (; m < m_tiles; ++m) v += static_cast<double>(p[static_cast<int64_t>(m) * D_out]);
+    col[static_cast<int64_t>(k) * D_out + n] = v;
+  }
+  sh[threadIdx.x] = v;
   __syncthreads();
   for (int w = kRedThreads / 2; w > 0; w >>= 1) {
     if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
     __syncthreads();
   }
-  if (threadIdx.x == 0) losses[k] = sh[0];
-}
-
-__global__ void argmin_copy_kernel(const double* __restrict__ losses, int G, const float* __restrict__ s_tab,
-                                   int64_t D_in, float* __restrict__ s_star, int32_t* __restrict__ best_idx,
-                                   uint32_t* status) {
-  __shared__ int kbest;
+  if (threadIdx.x == 0) {
+    blk[static_cast<int64_t>(k) * nb + blockIdx.x] = sh[0];
+    __threadfence();
+    const unsigned int done = atomicAdd(ticket, 1u);
+    last = done == static_cast<unsigned int>(nb) * static_cast<unsigned int>(G) - 1u;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (threadIdx.x < G) {
+    double L = 0.0;
+#pragma unroll 4
+    for (int b = 0; b < nb; ++b) L += blk[static_cast<int64_t>(threadIdx.x) * nb + b];
+    sh[threadIdx.x] = L;
+    losses[threadIdx.x] = L;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     int b = -1;
     double bl = 0.0;
-    for (int k = 0; k < G; ++k) {
-      const double L = losses[k];
+    for (int kk = 0; kk < G; ++kk) {
+      const double L = sh[kk];
       if (isnan(L)) continue;
       if (b < 0 || L < bl) {
-        b = k;
+        b = kk;
         bl = L;
       }
     }
@@ -57,25 +81,31 @@ __global__ void argmin_copy_kernel(const double* __restrict__ losses, int G, con
       set_error(status, AWQ_DEV_NONFINITE);
     }
     kbest = b;
-    if (blockIdx.x == 0) *best_idx = b;
+    *best_idx = b;
+    *ticket = 0u;  // ready for the next call on this workspace
   }
   __syncthreads();
   const float* src = s_tab + static_cast<int64_t>(kbest) * D_in;
-  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < D_in;
-       j += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    s_star[j] = src[j];
+  if ((reinterpret_cast<uintptr_t>(s_star) & 15u) == 0 && (D_in & 3) == 0) {
+    // s_tab rows start 16-byte aligned (D_in is a multiple of the group size)
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    float4* d4 = reinterpret_cast<float4*>(s_star);
+#pragma unroll 4
+    for (int64_t j = threadIdx.x; j < D_in / 4; j += kRedThreads) d4[j] = s4[j];
+  } else {
+    for (int64_t j = threadIdx.x; j < D_in; j += kRedThreads) s_star[j] = src[j];
+  }
 }
 
+int reduce_blocks(int64_t D_out) { return static_cast<int>((D_out + kRedThreads - 1) / kRedThreads); }
+
 cudaError_t launch_reduce_losses(const float* partial, int m_tiles, int64_t D_out, int G, double* col_losses,
-                                 double* losses, int32_t* best_idx, const float* s_tab, int64_t D_in, float* s_star,
-                                 uint32_t* status, cudaStream_t stream) {
-  const dim3 g1(static_cast<unsigned>((D_out + 255) / 256), static_cast<unsigned>(G));
-  reduce_rows_kernel<<<g1, 256, 0, stream>>>(partial, m_tiles, D_out, col_losses);
-  reduce_cols_kernel<<<G, kRedThreads, 0, stream>>>(col_losses, D_out, losses);
-  unsigned blocks = static_cast<unsigned>((D_in + 1023) / 1024);
-  if (blocks < 1) blocks = 1;
-  if (blocks > 64) blocks = 64;
-  argmin_copy_kernel<<<blocks, 1024, 0, stream>>>(losses, G, s_tab, D_in, s_star, best_idx, status);
+                                 double* blk, unsigned int* ticket, double* losses, int32_t* best_idx,
+                                 const float* s_tab, int64_t D_in, float* s_star, uint32_t* status,
+                                 cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(reduce_blocks(D_out)), static_cast<unsigned>(G));
+  reduce_losses_kernel<<<grid, kRedThreads, 0, stream>>>(partial, m_tiles, D_out, G, col_losses, blk, ticket, losses,
+                                                         best_idx, s_tab, D_in, s_star, status);
   return cudaGetLastError();
 }
 

@@ -53,7 +53,7 @@ constexpr int kWTileBytes = kBK * kHalfN * 2;   // 16 KB: 64 rows x 128 columns 
 constexpr int kSBytes = kBK * 4;                // s slice
 constexpr int kQBytes = (kHalfN / kQChunkCols) * kQChunkFloats * 4;  // step / zero chunks of 128 columns
 constexpr int kWStageTx = kWTileBytes + 2 * kSBytes + kQBytes;
-constexpr int kWStageStride = 19 * 1024;
+constexpr int kWStageStride = (kWStageTx + 127) / 128 * 128;  // TMA destinations stay 128-byte aligned
 constexpr int kOffB = kStages * kABytes;
 constexpr int kOffW = kOffB + kStages * kBBytes;
 constexpr int kSmemBytes = kOffW + kWStages * kWStageStride;
@@ -66,7 +66,7 @@ constexpr int kFullCount = 1 + 2 * kGroupWarps;  // TMA expect-tx + one producer
 constexpr int kAccEmptyCount = 2 * kEpiWarps;
 
 static_assert(kWTileBytes + 2 * kSBytes + kQBytes <= kWStageStride, "W stage");
-static_assert(kSmemBytes + 1024 <= 227 * 1024, "shared memory");
+static_assert(kSmemBytes + 1024 + 4608 <= 227 * 1024, "shared memory (dynamic + alignment slack + static)");
 
 struct FusedArgs {
   int N, D_in, D_out, G, T, group_size;

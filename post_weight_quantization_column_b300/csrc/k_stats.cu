@@ -53,15 +53,13 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_partial_kernel(const 
     const __nv_bfloat16* base = X + col;
     int64_t r = r0 + rl;
     constexpr int S = kStatsRowLanes;
-    for (; r + 3 * S < r1; r += 4 * S) {
-      const uint4 v0 = ld_stream_v4(base + r * ldx);
-      const uint4 v1 = ld_stream_v4(base + (r + S) * ldx);
-      const uint4 v2 = ld_stream_v4(base + (r + 2 * S) * ldx);
-      const uint4 v3 = ld_stream_v4(base + (r + 3 * S) * ldx);
-      add_abs_vec(v0, acc);
-      add_abs_vec(v1, acc);
-      add_abs_vec(v2, acc);
-      add_abs_vec(v3, acc);
+    // 8 rows in flight per thread
+    for (; r + 7 * S < r1; r += 8 * S) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = ld_stream_v4(base + (r + i * S) * ldx);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) add_abs_vec(v[i], acc);
     }
     for (; r < r1; r += S) add_abs_vec(ld_stream_v4(base + r * ldx), acc);
   }
@@ -84,7 +82,15 @@ __global__ void act_stats_final_kernel(const float* __restrict__ partial, int sp
   const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (j >= D) return;
   double s = 0.0;
-  for (int k = 0; k < splits; ++k) s += static_cast<double>(partial[static_cast<int64_t>(k) * D + j]);
+  int k = 0;
+  for (; k + 8 <= splits; k += 8) {
+    float v[8];  // eight loads in flight, added in slice order
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = partial[static_cast<int64_t>(k + i) * D + j];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += static_cast<double>(v[i]);
+  }
+  for (; k < splits; ++k) s += static_cast<double>(partial[static_cast<int64_t>(k) * D + j]);
   const float m = static_cast<float>(s / static_cast<double>(N));
   if (!isfinite(m)) set_error(status, AWQ_DEV_NONFINITE);
   mean_abs[j] = m;
