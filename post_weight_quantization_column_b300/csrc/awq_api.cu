@@ -30,6 +30,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 std::mutex g_mu;
 int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
 int g_pairs[kMaxDevices];    // resident CTA pairs of the fused search (0 = not queried)
+int g_sms[kMaxDevices];      // multiprocessor count (0 = not queried)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 awq_status check_device(int* dev_out) {
@@ -65,6 +66,17 @@ awq_status get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 }
 
 awq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA; }
+
+awq_status get_sms(int dev, int* sms) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return AWQ_ERR_CUDA;
+    g_sms[dev] = n;
+  }
+  *sms = g_sms[dev];
+  return AWQ_OK;
+}
 
 awq_status get_pairs(int dev, int* pairs) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -360,13 +372,20 @@ awq_status awq_quantize_pack(const void* W, const float* s, int64_t D_in, int64_
       !aligned(ws, 256))
     return AWQ_ERR_ALIGNMENT;
   if (ws_bytes < kHeaderBytes) return AWQ_ERR_WORKSPACE;
-  st = check_device(nullptr);
+  int dev = 0;
+  st = check_device(&dev);
+  if (st != AWQ_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  st = get_encode(&encode);
+  if (st != AWQ_OK) return st;
+  int sms = 0;
+  st = get_sms(dev, &sms);
   if (st != AWQ_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return AWQ_ERR_CUDA;
   ProfScope prof("pack", cs);
-  return from_cuda(launch_pack(W, s, D_in, D_out, cfg->group_size, cfg->symmetric, qweight, scales, zeros,
-                               status_word(ws), cs));
+  return from_cuda(launch_pack(encode, W, s, D_in, D_out, cfg->group_size, cfg->symmetric, qweight, scales, zeros,
+                               status_word(ws), sms, cs));
 }
 
 // ------------------------------------------------------------------ self-test GEMM

@@ -14,7 +14,7 @@ namespace awqdev {
 constexpr int kStatsThreads = 256;
 constexpr int kStatsRowLanes = 8;      // warps per CTA, each on its own rows
 constexpr int kStatsCols = 256;        // channels per CTA (32 lanes x 8)
-constexpr int kStatsTargetCtas = 148 * 2;
+constexpr int kStatsTargetCtas = 148 * 4;
 constexpr int kStatsMaxSplits = 1024;
 
 void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split);
@@ -49,8 +49,9 @@ cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in,
 cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r_tab, const float* qp,
                                int64_t D_in, int64_t D_out, int G, int group_size, int symmetric, void* dW,
                                cudaStream_t stream);
-cudaError_t launch_pack(const void* W, const float* s, int64_t D_in, int64_t D_out, int group_size, int symmetric,
-                        uint8_t* qweight, void* scales, void* zeros, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_pack(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* W, const float* s, int64_t D_in,
+                        int64_t D_out, int group_size, int symmetric, uint8_t* qweight, void* scales, void* zeros,
+                        uint32_t* status, int num_sms, cudaStream_t stream);
 
 // ----------------------------------------------------------------- search GEMM
 constexpr int kGemmBM = 128;

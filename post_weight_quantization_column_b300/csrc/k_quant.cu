@@ -1,5 +1,5 @@
-// Scale table, per-group quantiser parameters, candidate materialisation and
-// the bit-exact int4 pack.
+// Scale table, per-group quantiser parameters and candidate materialisation
+// (the bit-exact int4 pack is in k_pack.cu).
 //
 // Quantiser ("AWQ (Activation-aware Weight Quantization)", 技术原理 -
 // 量化数学基础; aiqz.cc article "awq-activation-aware-quantization", section 4;
@@ -8,8 +8,8 @@
 //               code = clamp(rint(w'/step) + zero, 0, 15)
 //   symmetric:  step = fp16(max|w'| / 7), code = clamp(rint(w'/step), -7, 7) (+8 when stored)
 //   dequant (code - zero) * step; a zero step gives dequant 0.
-// The pack reproduces the IEEE fp32 round-to-nearest quotient w'/step exactly;
-// the search uses a reciprocal multiply (its loss tolerance allows it).
+// The search uses a reciprocal multiply for w'/step (its loss tolerance
+// allows it); the pack reproduces the IEEE quotient exactly.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -304,227 +304,6 @@ cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r
                   static_cast<unsigned>(G));
   materialize_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(W), s_tab, r_tab, qp, D_in, D_out,
                                                group_size, lo, hi, static_cast<__nv_bfloat16*>(dW));
-  return cudaGetLastError();
-}
-
-// ------------------------------------------------------------------ pack
-// "AWQ (Activation-aware Weight Quantization)", 推理时的等效实现:
-// W_quantized = Quantize(diag(s*) W); "009. AWQ Integration", Consequences:
-// two 4-bit codes per byte (even input row in the low nibble).
-//
-// One CTA: one group (GS rows) x 64 columns, 256 threads.  Thread t owns the
-// 8 columns of chunk c = t % 8 and the row pairs (2p + 64i, 2p + 64i + 1),
-// p = t / 8, i < GS/64, so that both rows of a packed byte sit in one
-// thread.  Pass 1 finds the per-column range (shuffles over the 4 row slots
-// of a warp, then the 8 warps in a fixed order in shared memory) and the
-// exact step / zero; pass 2 emits codes.
-//
-// Codes equal clamp(rint(fp32(w'/step)) + zero): the quotient is first
-// formed as w' * (1/step); where that lands within 8e-6 of a half-integer
-// (where the two could round differently), the thread redoes its rows with
-// the IEEE division.  |w'/step| <= 45 in every case, where the product is
-// within 6e-6 of the IEEE quotient, so elsewhere both round alike.
-constexpr float kTieGuard = 0.5f - 8.0e-6f;
-constexpr int kPackCols = 64;
-
-template <int GS>
-__global__ void __launch_bounds__(256) pack_kernel(const __nv_bfloat16* __restrict__ W, const float* __restrict__ s,
-                                                 int64_t D_in, int64_t D_out, int symmetric,
-                                                 uint8_t* __restrict__ qweight, __half* __restrict__ scales,
-                                                 __half* __restrict__ zeros, uint32_t* status) {
-  constexpr int NP = GS / 64;  // row pairs per thread
-  constexpr int NR = 2 * NP;   // rows per thread
-  __shared__ float red_lo[8][kPackCols];
-  __shared__ float red_hi[8][kPackCols];
-  __shared__ float4 prm[kPackCols];  // {step, 1/step, zoff, zero}
-  const int t = threadIdx.x;
-  const int lane = t & 31;
-  const int wp_ = t >> 5;
-  const int c = t & 7;
-  const int pslot = t >> 3;
-  const int64_t n = static_cast<int64_t>(blockIdx.x) * kPackCols + c * 8;
-  const int64_t grp = blockIdx.y;
-  const int64_t jb = grp * GS + 2 * pslot;  // row pair i: jb + 64 i, jb + 64 i + 1
-  const bool active = n < D_out;
-
-  uint4 w[NR];
-  float sj[NR];
-  bool bad = false;
-#pragma unroll
-  for (int i = 0; i < NR; ++i) {
-    const int64_t row = jb + 64 * (i >> 1) + (i & 1);
-    sj[i] = s[row];
-    w[i] = active ? *reinterpret_cast<const uint4*>(W + row * D_out + n) : make_uint4(0u, 0u, 0u, 0u);
-    bad |= bf16x2_nonfinite(w[i].x) | bf16x2_nonfinite(w[i].y) | bf16x2_nonfinite(w[i].z) | bf16x2_nonfinite(w[i].w);
-  }
-  if (bad) set_error(status, AWQ_DEV_NONFINITE);
-
-  // pass 1: per-column range of w' = w * s over this thread's rows (two rows
-  // per step: packed products, three-input min / max)
-  float lo[8], hi[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) lo[k] = hi[k] = 0.f;
-#pragma unroll
-  for (int i = 0; i < NR; i += 2) {
-    const uint32_t we[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-    const uint32_t wo[4] = {w[i + 1].x, w[i + 1].y, w[i + 1].z, w[i + 1].w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 pe = __fmul2_rn(make_float2(bf16lo(we[k]), bf16hi(we[k])), make_float2(sj[i], sj[i]));
-      const float2 po = __fmul2_rn(make_float2(bf16lo(wo[k]), bf16hi(wo[k])), make_float2(sj[i + 1], sj[i + 1]));
-      if (symmetric) {
-        hi[2 * k] = fmaxabs3(hi[2 * k], pe.x, po.x);
-        hi[2 * k + 1] = fmaxabs3(hi[2 * k + 1], pe.y, po.y);
-      } else {
-        lo[2 * k] = fmin3(lo[2 * k], pe.x, po.x);
-        hi[2 * k] = fmax3(hi[2 * k], pe.x, po.x);
-        lo[2 * k + 1] = fmin3(lo[2 * k + 1], pe.y, po.y);
-        hi[2 * k + 1] = fmax3(hi[2 * k + 1], pe.y, po.y);
-      }
-    }
-  }
-  // lanes l, l^8, l^16, l^24 hold the same columns (four row slots)
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    lo[k] = fminf(lo[k], __shfl_xor_sync(0xFFFFFFFFu, lo[k], 8));
-    hi[k] = fmaxf(hi[k], __shfl_xor_sync(0xFFFFFFFFu, hi[k], 8));
-    lo[k] = fminf(lo[k], __shfl_xor_sync(0xFFFFFFFFu, lo[k], 16));
-    hi[k] = fmaxf(hi[k], __shfl_xor_sync(0xFFFFFFFFu, hi[k], 16));
-  }
-  if (lane < 8) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      red_lo[wp_][c * 8 + k] = lo[k];
-      red_hi[wp_][c * 8 + k] = hi[k];
-    }
-  }
-  __syncthreads();
-  if (t < kPackCols) {
-    const int col = t;
-    float l = 0.f, h = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      l = fminf(l, red_lo[k][col]);
-      h = fmaxf(h, red_hi[k][col]);
-    }
-    const float raw = symmetric ? __fdiv_rn(h, 7.0f) : __fdiv_rn(__fsub_rn(h, l), 15.0f);
-    float sc = __half2float(__float2half_rn(raw));
-    if (isinf(sc)) {
-      set_error(status, AWQ_DEV_RANGE);
-      sc = 0.f;
-    }
-    float z = 0.f;
-    if (!symmetric && sc != 0.f)
-      z = static_cast<float>(static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(-l, sc)), 0.f), 15.f)));
-    const float zoff = symmetric ? 8.f : z;
-    prm[col] = make_float4(sc, sc != 0.f ? __frcp_rn(sc) : 0.f, zoff, symmetric ? 8.f : z);
-    const int64_t ncol = static_cast<int64_t>(blockIdx.x) * kPackCols + col;
-    if (ncol < D_out) {
-      scales[grp * D_out + ncol] = __float2half_rn(sc);
-      zeros[grp * D_out + ncol] = __float2half_rn(symmetric ? 8.f : z);
-    }
-  }
-  __syncthreads();
-  if (!active) return;
-
-  float step[8], inv[8], zmz[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float4 pr = prm[c * 8 + k];
-    step[k] = pr.x;
-    inv[k] = pr.y;
-    zmz[k] = kMagic + pr.z;
-  }
-  const float clo = symmetric ? kMagic + 1.f : kMagic;
-  const float chi = kMagic + 15.f;
-
-  // pass 2 (fast): codes through the reciprocal.  y = w' (1/step); c =
-  // y + 1.5*2^23 + zero rounds it to an integer; tmax tracks the largest
-  // |y - rint(y)|, which flags a near tie anywhere in the thread's elements.
-  uint32_t out[NP][2];
-  float tmax = 0.f;
-#pragma unroll
-  for (int i = 0; i < NP; ++i) {
-    const uint32_t we[4] = {w[2 * i].x, w[2 * i].y, w[2 * i].z, w[2 * i].w};
-    const uint32_t wo[4] = {w[2 * i + 1].x, w[2 * i + 1].y, w[2 * i + 1].z, w[2 * i + 1].w};
-    uint32_t bytes[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 inv2 = make_float2(inv[2 * k], inv[2 * k + 1]);
-      const float2 zm2 = make_float2(zmz[2 * k], zmz[2 * k + 1]);
-      const float2 nzm2 = make_float2(-zmz[2 * k], -zmz[2 * k + 1]);
-      const float2 ye = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(we[k]), bf16hi(we[k])), make_float2(sj[2 * i], sj[2 * i])), inv2);
-      const float2 yo = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(wo[k]), bf16hi(wo[k])), make_float2(sj[2 * i + 1], sj[2 * i + 1])), inv2);
-      float2 ce = __fadd2_rn(ye, zm2);
-      float2 co = __fadd2_rn(yo, zm2);
-      const float2 de = __ffma2_rn(ye, make_float2(-1.f, -1.f), __fadd2_rn(ce, nzm2));
-      const float2 dd = __ffma2_rn(yo, make_float2(-1.f, -1.f), __fadd2_rn(co, nzm2));
-      tmax = fmaxabs3(tmax, de.x, de.y);
-      tmax = fmaxabs3(tmax, dd.x, dd.y);
-      ce.x = fminf(fmaxf(ce.x, clo), chi);
-      ce.y = fminf(fmaxf(ce.y, clo), chi);
-      co.x = fminf(fmaxf(co.x, clo), chi);
-      co.y = fminf(fmaxf(co.y, clo), chi);
-      bytes[2 * k] = (__float_as_uint(ce.x) & 0xFu) | ((__float_as_uint(co.x) & 0xFu) << 4);
-      bytes[2 * k + 1] = (__float_as_uint(ce.y) & 0xFu) | ((__float_as_uint(co.y) & 0xFu) << 4);
-    }
-    out[i][0] = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
-    out[i][1] = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
-  }
-  const bool tie = tmax > kTieGuard;
-  if (tie) {
-    // slow path: IEEE quotient for every element of this thread
-#pragma unroll
-    for (int i = 0; i < NP; ++i) {
-      const uint32_t we[4] = {w[2 * i].x, w[2 * i].y, w[2 * i].z, w[2 * i].w};
-      const uint32_t wo[4] = {w[2 * i + 1].x, w[2 * i + 1].y, w[2 * i + 1].z, w[2 * i + 1].w};
-      uint32_t bytes[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float xe = (k & 1) ? bf16hi(we[k >> 1]) : bf16lo(we[k >> 1]);
-        const float xo = (k & 1) ? bf16hi(wo[k >> 1]) : bf16lo(wo[k >> 1]);
-        // clamp(rint(IEEE w'/step) + zoff, clo, 15); a zero step keeps code zoff
-        uint32_t ke = static_cast<uint32_t>(zmz[k] - kMagic), ko = ke;
-        if (step[k] != 0.f) {
-          const float zo = zmz[k] - kMagic;
-          const float ql = clo - kMagic;
-          const float qe = rintf(__fdiv_rn(__fmul_rn(xe, sj[2 * i]), step[k])) + zo;
-          const float qo = rintf(__fdiv_rn(__fmul_rn(xo, sj[2 * i + 1]), step[k])) + zo;
-          ke = static_cast<uint32_t>(fminf(fmaxf(qe, ql), 15.f));
-          ko = static_cast<uint32_t>(fminf(fmaxf(qo, ql), 15.f));
-        }
-        bytes[k] = ke | (ko << 4);
-      }
-      out[i][0] = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
-      out[i][1] = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < NP; ++i) {
-    const int64_t prow = (jb + 64 * i) / 2;
-    *reinterpret_cast<uint2*>(qweight + prow * D_out + n) = make_uint2(out[i][0], out[i][1]);
-  }
-}
-
-cudaError_t launch_pack(const void* W, const float* s, int64_t D_in, int64_t D_out, int group_size, int symmetric,
-                        uint8_t* qweight, void* scales, void* zeros, uint32_t* status, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>((D_out + kPackCols - 1) / kPackCols), static_cast<unsigned>(D_in / group_size));
-  const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
-  __half* sc = static_cast<__half*>(scales);
-  __half* zr = static_cast<__half*>(zeros);
-  switch (group_size) {
-    case 64:
-      pack_kernel<64><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
-      break;
-    case 128:
-      pack_kernel<128><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
-      break;
-    case 256:
-      pack_kernel<256><<<grid, 256, 0, stream>>>(Wb, s, D_in, D_out, symmetric, qweight, sc, zr, status);
-      break;
-    default:
-      return cudaErrorInvalidValue;
-  }
   return cudaGetLastError();
 }
 

@@ -62,6 +62,7 @@ constexpr int kThreads = 640;
 constexpr int kEpiWarp0 = 4, kEpiWarps = 8;
 constexpr int kProdWarp0 = 12, kProdWarps = 8;
 constexpr int kGroupWarps = 4;                   // producer warps per K step (two groups alternate)
+static_assert(kProdWarps == 2 * kGroupWarps, "two producer groups");
 constexpr int kFullCount = 1 + 2 * kGroupWarps;  // TMA expect-tx + one producer group of each CTA
 constexpr int kAccEmptyCount = 2 * kEpiWarps;
 
