@@ -117,9 +117,11 @@ AWQ_API awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t
  * host program that has already reserved all device memory for its own pool
  * and exposes no allocator, or code on a latency-critical path that must not
  * call cudaMalloc (which can synchronise the whole device).  This entry point
- * takes only X and the output; its scratch (the per-row-slice partial sums)
- * is a 4 MiB array of static device memory inside the library, which every
- * device that loads the library holds until the process exits.
+ * takes only X and the output; its scratch (the per-row-slice partial sums
+ * and one completion counter per 256 channels) is a 4 MiB + 16 KiB array of
+ * static device memory inside the library, which every device that loads the
+ * library holds until the process exits.  Each call clears the counters it
+ * uses (cudaMemsetAsync on the array, which allocates nothing).
  *
  *   X, N, D_in, ldx, mean_abs  as for awq_act_stats
  * Limits: D_in <= 1048576 channels (one row slice must fit the array);

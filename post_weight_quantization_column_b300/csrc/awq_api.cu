@@ -158,11 +158,13 @@ awq_status validate_cfg(const awq_cfg* cfg) {
 uint32_t* status_word(void* ws) { return static_cast<uint32_t*>(ws); }
 
 // ---------------------------------------------------------------- layouts
+// act_stats workspace: header (status word) | tickets [stats_chunks] | partials [splits][D_in]
+size_t stats_ticket_bytes(int64_t D_in) { return align_up(static_cast<size_t>(stats_chunks(D_in)) * 4, 256); }
 size_t stats_ws_bytes(int64_t N, int64_t D_in) {
   int splits = 1;
   int64_t rps = 0;
   stats_plan(N, D_in, &splits, &rps);
-  return kHeaderBytes + align_up(static_cast<size_t>(splits) * static_cast<size_t>(D_in) * 4, 256);
+  return kHeaderBytes + stats_ticket_bytes(D_in) + align_up(static_cast<size_t>(splits) * static_cast<size_t>(D_in) * 4, 256);
 }
 
 struct SearchLayout {
@@ -258,10 +260,13 @@ awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t ldx, fl
   int splits = 1;
   int64_t rps = 0;
   stats_plan(N, D_in, &splits, &rps);
-  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return AWQ_ERR_CUDA;
-  float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
+  // status word and the ticket counters start at zero
+  const size_t tb = stats_ticket_bytes(D_in);
+  if (cudaMemsetAsync(ws, 0, kHeaderBytes + tb, s) != cudaSuccess) return AWQ_ERR_CUDA;
+  unsigned int* tickets = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
+  float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kHeaderBytes + tb);
   ProfScope prof("act_stats", s);
-  return from_cuda(launch_act_stats(X, N, D_in, ldx, mean_abs, partial, splits, rps, status_word(ws), s));
+  return from_cuda(launch_act_stats(X, N, D_in, ldx, mean_abs, partial, tickets, splits, rps, status_word(ws), s));
 }
 
 // ------------------------------------------------------------------ search

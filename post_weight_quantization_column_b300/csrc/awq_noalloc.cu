@@ -9,11 +9,13 @@
 
 namespace {
 
-// 4 MiB of fp32 partial sums, held by every device that loads the library
-// until the process exits.  One slice of D_in channels must fit, so D_in is
-// limited to kNoAllocScratchFloats.
+// 4 MiB of fp32 partial sums plus 16 KiB of per-chunk ticket counters in
+// front of them, held by every device that loads the library until the
+// process exits.  One slice of D_in channels must fit, so D_in is limited to
+// kNoAllocScratchFloats.
 constexpr int64_t kNoAllocScratchFloats = int64_t(1) << 20;
-static __device__ __align__(256) float g_stats_scratch[kNoAllocScratchFloats];
+constexpr int64_t kNoAllocTicketWords = kNoAllocScratchFloats / 256;  // one per 256-channel chunk
+static __device__ __align__(256) float g_stats_scratch[kNoAllocTicketWords + kNoAllocScratchFloats];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
@@ -66,10 +68,16 @@ extern "C" awq_status awq_act_stats_noalloc(const void* X, int64_t N, int64_t D_
     rps = (rps + awqdev::kStatsRowLanes - 1) / awqdev::kStatsRowLanes * awqdev::kStatsRowLanes;
     splits = static_cast<int>((N + rps - 1) / rps);
   }
-  // Every partial the final pass reads is rewritten by this call, so nothing
-  // has to be cleared; there is no status word (a non-finite X shows up as a
-  // non-finite mean).
-  const cudaError_t e = awqdev::launch_act_stats(X, N, D_in, ldx, mean_abs, scratch, splits, rps, nullptr,
-                                                 reinterpret_cast<cudaStream_t>(stream));
+  // Every partial the final sums read is rewritten by this call; the ticket
+  // counters must start at zero (the kernel leaves them zero, and the array
+  // starts zeroed, but clearing them here keeps each call self-contained).
+  // There is no status word: a non-finite X shows up as a non-finite mean.
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int* tickets = reinterpret_cast<unsigned int*>(scratch);
+  const int64_t chunks = awqdev::stats_chunks(D_in);
+  if (cudaMemsetAsync(tickets, 0, static_cast<size_t>(chunks) * sizeof(unsigned int), s) != cudaSuccess)
+    return AWQ_ERR_CUDA;
+  const cudaError_t e = awqdev::launch_act_stats(X, N, D_in, ldx, mean_abs, scratch + kNoAllocTicketWords, tickets,
+                                                 splits, rps, nullptr, s);
   return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
 }

@@ -18,8 +18,13 @@ constexpr int kStatsTargetCtas = 148 * 4;
 constexpr int kStatsMaxSplits = 1024;
 
 void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split);
+// Column chunks of 256 channels: the number of ticket counters the kernel uses.
+int64_t stats_chunks(int64_t D);
+// partial: fp32 [splits][D] scratch; tickets: uint32 [stats_chunks(D)], zero on
+// entry (the kernel leaves them zero again).
 cudaError_t launch_act_stats(const void* X, int64_t N, int64_t D, int64_t ldx, float* mean_abs, float* partial,
-                             int splits, int64_t rows_per_split, uint32_t* status, cudaStream_t stream);
+                             unsigned int* tickets, int splits, int64_t rows_per_split, uint32_t* status,
+                             cudaStream_t stream);
 
 // ----------------------------------------------------------------- quantiser
 constexpr int kMaxGrid = 64;

@@ -7,7 +7,8 @@
 // reads 512 contiguous bytes per row; the 8 warps take interleaved rows of the
 // CTA's row slice.  Per-thread sums are fp32, the 8 warps are combined in a
 // fixed order through shared memory, and the row slices are summed in fp64 in
-// slice order by a second kernel, so the result does not depend on timing.
+// slice order by the last CTA of each column chunk to finish (a per-chunk
+// ticket counter), so the result does not depend on timing.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -36,11 +37,13 @@ __device__ __forceinline__ void add_abs_vec(const uint4& v, float (&acc)[8]) {
   add_abs_pair(v.w, acc[6], acc[7]);
 }
 
-__global__ void __launch_bounds__(kStatsThreads) act_stats_partial_kernel(const __nv_bfloat16* __restrict__ X,
-                                                                         int64_t N, int64_t D, int64_t ldx,
-                                                                         int64_t rows_per_split,
-                                                                         float* __restrict__ partial) {
+__global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __nv_bfloat16* __restrict__ X, int64_t N,
+                                                                 int64_t D, int64_t ldx, int64_t rows_per_split,
+                                                                 float* __restrict__ partial,
+                                                                 unsigned int* __restrict__ tickets,
+                                                                 float* __restrict__ mean_abs, uint32_t* status) {
   __shared__ __align__(16) float red[kStatsRowLanes][kStatsCols];
+  __shared__ bool last;
   const int lane = threadIdx.x & 31;
   const int rl = threadIdx.x >> 5;
   const int64_t col = static_cast<int64_t>(blockIdx.x) * kStatsCols + lane * 8;
@@ -70,30 +73,35 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_partial_kernel(const 
   const int t = threadIdx.x;
   const int64_t j = static_cast<int64_t>(blockIdx.x) * kStatsCols + t;
   if (t < kStatsCols && j < D) {
-    float s = 0.f;
+    float sum = 0.f;
 #pragma unroll
-    for (int k = 0; k < kStatsRowLanes; ++k) s += red[k][t];
-    partial[static_cast<int64_t>(blockIdx.y) * D + j] = s;
+    for (int k = 0; k < kStatsRowLanes; ++k) sum += red[k][t];
+    partial[static_cast<int64_t>(blockIdx.y) * D + j] = sum;
   }
-}
-
-__global__ void act_stats_final_kernel(const float* __restrict__ partial, int splits, int64_t D, int64_t N,
-                                       float* __restrict__ mean_abs, uint32_t* status) {
-  const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (j >= D) return;
-  double s = 0.0;
-  int k = 0;
-  for (; k + 8 <= splits; k += 8) {
-    float v[8];  // eight loads in flight, added in slice order
+  // the last row slice of this column chunk to finish sums the slices
+  __threadfence();
+  __syncthreads();
+  if (t == 0) last = atomicAdd(&tickets[blockIdx.x], 1u) == gridDim.y - 1u;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (t < kStatsCols && j < D) {
+    const int splits = static_cast<int>(gridDim.y);
+    double s = 0.0;
+    int k = 0;
+    for (; k + 8 <= splits; k += 8) {
+      float v[8];  // eight loads in flight, added in slice order
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = partial[static_cast<int64_t>(k + i) * D + j];
+      for (int i = 0; i < 8; ++i) v[i] = partial[static_cast<int64_t>(k + i) * D + j];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s += static_cast<double>(v[i]);
+      for (int i = 0; i < 8; ++i) s += static_cast<double>(v[i]);
+    }
+    for (; k < splits; ++k) s += static_cast<double>(partial[static_cast<int64_t>(k) * D + j]);
+    const float m = static_cast<float>(s / static_cast<double>(N));
+    if (!isfinite(m)) set_error(status, AWQ_DEV_NONFINITE);
+    mean_abs[j] = m;
   }
-  for (; k < splits; ++k) s += static_cast<double>(partial[static_cast<int64_t>(k) * D + j]);
-  const float m = static_cast<float>(s / static_cast<double>(N));
-  if (!isfinite(m)) set_error(status, AWQ_DEV_NONFINITE);
-  mean_abs[j] = m;
+  if (t == 0) tickets[blockIdx.x] = 0u;  // ready for the next call
 }
 
 void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split) {
@@ -112,14 +120,14 @@ void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split) {
 }
 
 cudaError_t launch_act_stats(const void* X, int64_t N, int64_t D, int64_t ldx, float* mean_abs, float* partial,
-                             int splits, int64_t rows_per_split, uint32_t* status, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>((D + kStatsCols - 1) / kStatsCols), static_cast<unsigned>(splits));
-  act_stats_partial_kernel<<<grid, kStatsThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(X), N, D, ldx,
-                                                              rows_per_split, partial);
-  const int fin_threads = 256;
-  act_stats_final_kernel<<<static_cast<unsigned>((D + fin_threads - 1) / fin_threads), fin_threads, 0, stream>>>(
-      partial, splits, D, N, mean_abs, status);
+                             unsigned int* tickets, int splits, int64_t rows_per_split, uint32_t* status,
+                             cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(stats_chunks(D)), static_cast<unsigned>(splits));
+  act_stats_kernel<<<grid, kStatsThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(X), N, D, ldx, rows_per_split,
+                                                       partial, tickets, mean_abs, status);
   return cudaGetLastError();
 }
+
+int64_t stats_chunks(int64_t D) { return (D + kStatsCols - 1) / kStatsCols; }
 
 }  // namespace awqdev
