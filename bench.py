@@ -27,9 +27,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "AWQ alpha-search TFLOP/s & layers/sec (21-pt grid) vs tensor-pipe peak; pack GB/s"
-KERNELS_PER_LAUNCHER = {"act_stats": 1, "scale_table": 1, "group_params": 1, "materialize": 1,
-                        "search_gemm": 1, "search_fused": 1, "reduce_argmin": 1, "pack": 1}
-SEARCH_KERNELS = ("search_fused", "search_gemm")
+KERNELS_PER_LAUNCHER = {"act_stats": 1, "scale_table": 1, "group_params": 1, "search_fused": 1,
+                        "reduce_argmin": 1, "pack": 1}
+SEARCH_KERNELS = ("search_fused",)
 
 
 def parse_args(argv=None):

@@ -89,17 +89,6 @@ awq_status get_pairs(int dev, int* pairs) {
   return AWQ_OK;
 }
 
-// Development comparison: AWQ_SEARCH_IMPL=materialized selects the path that
-// writes every candidate matrix to the workspace and runs a plain GEMM over it.
-bool materialized_search() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = std::getenv("AWQ_SEARCH_IMPL");
-    v = (e && std::strcmp(e, "materialized") == 0) ? 1 : 0;
-  }
-  return v == 1;
-}
-
 // ---------------------------------------------------------------- optional event timing
 struct ProfRecord {
   std::string name;
@@ -168,7 +157,7 @@ size_t stats_ws_bytes(int64_t N, int64_t D_in) {
 }
 
 struct SearchLayout {
-  size_t s_tab, r_tab, qp, partial, col, blk, dW, total;
+  size_t s_tab, r_tab, qp, partial, col, blk, total;
   int m_tiles;
 };
 
@@ -176,8 +165,7 @@ SearchLayout search_layout(int64_t N, int64_t D_in, int64_t D_out, int G, int gr
   SearchLayout L;
   const size_t g = static_cast<size_t>(G);
   const size_t din = static_cast<size_t>(D_in), dout = static_cast<size_t>(D_out);
-  const bool mat = materialized_search();
-  L.m_tiles = mat ? static_cast<int>((N + kGemmBM - 1) / kGemmBM) : search_fused_m_tiles(N);
+  L.m_tiles = search_fused_m_tiles(N);
   size_t off = kHeaderBytes;
   L.s_tab = off;
   off = align_up(off + g * din * 4, 256);
@@ -191,8 +179,6 @@ SearchLayout search_layout(int64_t N, int64_t D_in, int64_t D_out, int G, int gr
   off = align_up(off + g * dout * 8, 256);
   L.blk = off;
   off = align_up(off + g * static_cast<size_t>(reduce_blocks(D_out)) * 8, 256);
-  L.dW = off;
-  if (mat) off = align_up(off + g * din * dout * 2, 256);
   L.total = off;
   return L;
 }
@@ -204,7 +190,7 @@ awq_status validate_search_shape(int64_t N, int64_t D_in, int64_t D_out, int32_t
   if (N < 1 || D_in < 1 || D_out < 1) return AWQ_ERR_SHAPE;
   if (D_in % cfg->group_size != 0 || D_out % 8 != 0) return AWQ_ERR_SHAPE;
   const int64_t lim = (int64_t(1) << 31) - 1;
-  if (N > int64_t(65535) * kGemmBM || D_in > lim / G || D_out > lim) return AWQ_ERR_SHAPE;
+  if (N > lim || D_in > lim / G || D_out > lim) return AWQ_ERR_SHAPE;
   return AWQ_OK;
 }
 
@@ -302,12 +288,9 @@ awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   st = get_encode(&encode);
   if (st != AWQ_OK) return st;
-  const bool mat = materialized_search();
   int pairs = 0;
-  if (!mat) {
-    st = get_pairs(dev, &pairs);
-    if (st != AWQ_OK) return st;
-  }
+  st = get_pairs(dev, &pairs);
+  if (st != AWQ_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -317,7 +300,6 @@ awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int
   float* qp = reinterpret_cast<float*>(base + L.qp);
   float* partial = reinterpret_cast<float*>(base + L.partial);
   double* col = col_losses ? col_losses : reinterpret_cast<double*>(base + L.col);
-  void* dW = base + L.dW;
 
   // status word and the reduction's ticket counter
   if (cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return AWQ_ERR_CUDA;
@@ -330,16 +312,7 @@ awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int
     ProfScope prof("group_params", s);
     e = launch_group_params(W, s_tab, D_in, D_out, G, cfg->group_size, cfg->symmetric, qp, status, s);
   }
-  if (mat) {
-    if (e == cudaSuccess) {
-      ProfScope prof("materialize", s);
-      e = launch_materialize(W, s_tab, r_tab, qp, D_in, D_out, G, cfg->group_size, cfg->symmetric, dW, s);
-    }
-    if (e == cudaSuccess) {
-      ProfScope prof("search_gemm", s);
-      e = launch_gemm_ssq(encode, X, dW, N, D_out, D_in, G, partial, status, s);
-    }
-  } else if (e == cudaSuccess) {
+  if (e == cudaSuccess) {
     ProfScope prof("search_fused", s);
     e = launch_search_fused(encode, X, W, s_tab, r_tab, qp, N, D_in, D_out, G, cfg->group_size, cfg->symmetric,
                             partial, status, pairs, s);

@@ -51,23 +51,17 @@ cudaError_t launch_scale_table(const float* mean_abs, int64_t D_in, const AlphaG
                                float* s_tab, float* r_tab, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in, int64_t D_out, int G,
                                 int group_size, int symmetric, float* qp, uint32_t* status, cudaStream_t stream);
-cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r_tab, const float* qp,
-                               int64_t D_in, int64_t D_out, int G, int group_size, int symmetric, void* dW,
-                               cudaStream_t stream);
 cudaError_t launch_pack(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* W, const float* s, int64_t D_in,
                         int64_t D_out, int group_size, int symmetric, uint8_t* qweight, void* scales, void* zeros,
                         uint32_t* status, int num_sms, cudaStream_t stream);
 
-// ----------------------------------------------------------------- search GEMM
+// ----------------------------------------------------------------- tensor-core self-test
 constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 64;
 
-size_t gemm_smem_bytes();
-// out_partial: [Z][m_tiles][N] per-column sums of squares of X * B_z.
-cudaError_t launch_gemm_ssq(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* A, const void* B, int64_t M,
-                            int64_t N, int64_t K, int Z, float* out_partial, uint32_t* status, cudaStream_t stream);
-// Plain C = A * B in fp32 (self-test of the tensor-core main loop).
+// Plain C = A * B in fp32 through a tcgen05 main loop (TMA ring, TMEM
+// accumulator): the self-test of the UMMA descriptors the search relies on.
 cudaError_t launch_gemm_store(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* A, const void* B, int b_mn_major,
                               int64_t M, int64_t N, int64_t K, float* C, uint32_t* status, cudaStream_t stream);
 

@@ -1,16 +1,13 @@
-// Tensor-core main loop of the candidate search (sm_103a, tcgen05 + TMA).
+// Plain tensor-core GEMM (sm_103a, tcgen05 + TMA): the self-test of the
+// UMMA machinery the fused search relies on (shared-memory descriptors with
+// 128-byte swizzle for a K-major A and an N-major or K-major B, the
+// instruction descriptor, TMEM allocation and tcgen05.ld).  One CTA computes
+// a 128 x 256 tile of C = A * B:
 //
-// For candidate z the search needs the output error E_z = X * dW_z with
-// dW_z = S_z^-1 W'hat_z - W ("AWQ (Activation-aware Weight Quantization)",
-// 缩放因子优化的完整流程 step 4c, written in difference form), and only its
-// per-column sums of squares.  One CTA computes a 128 x 256 tile of E_z:
-//
-//   warp 0      TMA producer: X tile (128 rows x 64 K, K-major, 128B swizzle)
-//               and dW tile (64 K x 256 N, N-major, 128B swizzle) per stage
+//   warp 0      TMA producer: A tile (128 rows x 64 K, K-major, 128B swizzle)
+//               and B tile (64 K x 256 N) per stage
 //   warp 1      TMEM allocation and the single-thread tcgen05.mma issue loop
-//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator, square, sum over
-//               the 128 rows (warp transpose-reduce, then the 4 warps in a
-//               fixed order), one fp32 partial per column
+//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator, stored to C
 //
 // A 4-stage mbarrier ring connects TMA and MMA; every wait is bounded.
 #include <cuda_bf16.h>
@@ -31,34 +28,15 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = BN;                // fp32 accumulator 128 lanes x 256 columns
 constexpr int kGemmThreads = 192;
 
-size_t gemm_smem_bytes() { return static_cast<size_t>(kStages) * kStageBytes + 1024; }
-
-enum { kEpiSsq = 0, kEpiStore = 1 };
+static size_t gemm_smem_bytes() { return static_cast<size_t>(kStages) * kStageBytes + 1024; }
 
 struct GemmArgs {
   int M, N, K;
-  int m_tiles;
-  int b_rows_per_z;     // row offset of candidate z inside the B tensor (N-major B)
   float* out;
   uint32_t* status;
 };
 
-// Sum v[0..31] across the 32 lanes so that lane l ends with sum_lanes v[l].
-__device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const bool upper = (lane & off) != 0;
-#pragma unroll
-    for (int i = 0; i < off; ++i) {
-      const float send = upper ? v[i] : v[i + off];
-      const float keep = upper ? v[i + off] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
-    }
-  }
-  return v[0];
-}
-
-template <int EPI, int B_MN>
+template <int B_MN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         GemmArgs p) {
@@ -71,14 +49,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __shared__ __align__(8) uint64_t acc_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ float red[4][BN];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
-  const int m_tile = blockIdx.y;
-  const int m0 = m_tile * BM;
-  const int z = blockIdx.z;
+  const int m0 = blockIdx.y * BM;
   const int num_kb = p.K / BK;
 
   if (threadIdx.x == 0) {
@@ -114,8 +89,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (B_MN) {
 #pragma unroll
         for (int i = 0; i < BN / 64; ++i)
-          tma_load_2d(sB + s * kBBytes + i * kBBoxBytes, &tmB, &full_bar[s], n0 + 64 * i,
-                      z * p.b_rows_per_z + kb * BK);
+          tma_load_2d(sB + s * kBBytes + i * kBBoxBytes, &tmB, &full_bar[s], n0 + 64 * i, kb * BK);
       } else {
         tma_load_2d(sB + s * kBBytes, &tmB, &full_bar[s], kb * BK, n0);
       }
@@ -163,29 +137,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int c = 0; c < BN; c += 32) {
         float v[32];
         tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
-        if (EPI == kEpiStore) {
-          if (row < p.M) {
+        if (row < p.M) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (n0 + c + i < p.N) p.out[static_cast<int64_t>(row) * p.N + n0 + c + i] = v[i];
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= v[i];
-          red[q][c + lane] = warp_transpose_sum(v, lane);
+          for (int i = 0; i < 32; ++i)
+            if (n0 + c + i < p.N) p.out[static_cast<int64_t>(row) * p.N + n0 + c + i] = v[i];
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (EPI == kEpiSsq && !abort_sh) {
-    for (int col = threadIdx.x; col < BN; col += kGemmThreads) {
-      const float sum = ((red[0][col] + red[1][col]) + red[2][col]) + red[3][col];
-      if (n0 + col < p.N)
-        p.out[(static_cast<int64_t>(z) * p.m_tiles + m_tile) * p.N + n0 + col] = sum;
-    }
-  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -205,45 +166,36 @@ static cudaError_t encode_2d_bf16(PFN_cuTensorMapEncodeTiled_v12000 encode, CUte
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int EPI, int B_MN>
+template <int B_MN>
 static cudaError_t launch_gemm_impl(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* A, const void* B,
-                                    int64_t M, int64_t N, int64_t K, int Z, int64_t b_rows_total, float* out,
-                                    uint32_t* status, cudaStream_t stream) {
+                                    int64_t M, int64_t N, int64_t K, float* out, uint32_t* status, cudaStream_t stream) {
   CUtensorMap tmA, tmB;
   cudaError_t e = encode_2d_bf16(encode, &tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), BK, BM);
   if (e != cudaSuccess) return e;
   if (B_MN)
-    e = encode_2d_bf16(encode, &tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(b_rows_total), 64, BK);
+    e = encode_2d_bf16(encode, &tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 64, BK);
   else
     e = encode_2d_bf16(encode, &tmB, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), BK, BN);
   if (e != cudaSuccess) return e;
   const size_t smem = gemm_smem_bytes();
-  e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   GemmArgs a;
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
-  a.m_tiles = static_cast<int>((M + BM - 1) / BM);
-  a.b_rows_per_z = static_cast<int>(K);
   a.out = out;
   a.status = status;
-  const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>(a.m_tiles), static_cast<unsigned>(Z));
-  gemm_bf16_tc_kernel<EPI, B_MN><<<grid, kGemmThreads, smem, stream>>>(tmA, tmB, a);
+  const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM), 1);
+  gemm_bf16_tc_kernel<B_MN><<<grid, kGemmThreads, smem, stream>>>(tmA, tmB, a);
   return cudaGetLastError();
-}
-
-cudaError_t launch_gemm_ssq(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* A, const void* B, int64_t M,
-                            int64_t N, int64_t K, int Z, float* out_partial, uint32_t* status, cudaStream_t stream) {
-  return launch_gemm_impl<kEpiSsq, 1>(encode, A, B, M, N, K, Z, static_cast<int64_t>(Z) * K, out_partial, status,
-                                      stream);
 }
 
 cudaError_t launch_gemm_store(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* A, const void* B, int b_mn_major,
                               int64_t M, int64_t N, int64_t K, float* C, uint32_t* status, cudaStream_t stream) {
-  if (b_mn_major) return launch_gemm_impl<kEpiStore, 1>(encode, A, B, M, N, K, 1, K, C, status, stream);
-  return launch_gemm_impl<kEpiStore, 0>(encode, A, B, M, N, K, 1, N, C, status, stream);
+  if (b_mn_major) return launch_gemm_impl<1>(encode, A, B, M, N, K, C, status, stream);
+  return launch_gemm_impl<0>(encode, A, B, M, N, K, C, status, stream);
 }
 
 }  // namespace awqdev

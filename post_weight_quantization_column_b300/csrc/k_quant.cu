@@ -1,5 +1,5 @@
-// Scale table, per-group quantiser parameters and candidate materialisation
-// (the bit-exact int4 pack is in k_pack.cu).
+// Scale table and per-group quantiser parameters of the search (the
+// bit-exact int4 pack is in k_pack.cu).
 //
 // Quantiser ("AWQ (Activation-aware Weight Quantization)", 技术原理 -
 // 量化数学基础; aiqz.cc article "awq-activation-aware-quantization", section 4;
@@ -240,71 +240,6 @@ cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in,
     default:
       return cudaErrorInvalidValue;
   }
-}
-
-// ------------------------------------------------------------------ candidate materialisation
-// dW_k[j, n] = bf16( (code - zero) * step / s_kj - w_jn ): the difference form
-// S^-1 W'hat - W of one candidate, so that X * dW_k is the output error of
-// "AWQ (Activation-aware Weight Quantization)", 缩放因子优化的完整流程 step 4c.
-__device__ __forceinline__ float dq_delta(float w, float s, float r, const QParam& q, float lo, float hi) {
-  const float wp = w * s;
-  float t = fmaf(wp, q.inv, q.zm);
-  t = fminf(fmaxf(t, lo), hi);
-  const float d = (t - q.zm) * q.step;
-  return fmaf(d, r, -w);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-__global__ void __launch_bounds__(256) materialize_kernel(const __nv_bfloat16* __restrict__ W,
-                                                        const float* __restrict__ s_tab,
-                                                        const float* __restrict__ r_tab,
-                                                        const float* __restrict__ qp, int64_t D_in, int64_t D_out,
-                                                        int group_size, float lo, float hi,
-                                                        __nv_bfloat16* __restrict__ dW) {
-  const int lane = threadIdx.x & 31;
-  const int rl = threadIdx.x >> 5;
-  const int64_t n = static_cast<int64_t>(blockIdx.x) * 256 + lane * 8;
-  if (n >= D_out) return;
-  const int k = blockIdx.z;
-  const int64_t jb = static_cast<int64_t>(blockIdx.y) * 64;
-  const int64_t T = D_in / group_size;
-  const int64_t grp = jb / group_size;
-  const float* q = qp + ((static_cast<int64_t>(k) * T + grp) * (D_out / kQChunkCols) + n / kQChunkCols) * kQChunkFloats;
-  QParam qv[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) qv[c] = QParam{q[c], q[kQChunkCols + c], q[2 * kQChunkCols + c], 0.f};
-#pragma unroll 2
-  for (int i = 0; i < 8; ++i) {
-    const int64_t j = jb + rl + 8 * i;
-    const float s = s_tab[static_cast<int64_t>(k) * D_in + j];
-    const float r = r_tab[static_cast<int64_t>(k) * D_in + j];
-    const uint4 wv = *reinterpret_cast<const uint4*>(W + j * D_out + n);
-    const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float d0 = dq_delta(bf16lo(wu[c]), s, r, qv[2 * c], lo, hi);
-      const float d1 = dq_delta(bf16hi(wu[c]), s, r, qv[2 * c + 1], lo, hi);
-      o[c] = pack_bf16x2(d0, d1);
-    }
-    *reinterpret_cast<uint4*>(dW + (static_cast<int64_t>(k) * D_in + j) * D_out + n) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
-
-cudaError_t launch_materialize(const void* W, const float* s_tab, const float* r_tab, const float* qp,
-                               int64_t D_in, int64_t D_out, int G, int group_size, int symmetric, void* dW,
-                               cudaStream_t stream) {
-  const float lo = symmetric ? kMagic - 7.f : kMagic;
-  const float hi = symmetric ? kMagic + 7.f : kMagic + 15.f;
-  const dim3 grid(static_cast<unsigned>((D_out + 255) / 256), static_cast<unsigned>(D_in / 64),
-                  static_cast<unsigned>(G));
-  materialize_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(W), s_tab, r_tab, qp, D_in, D_out,
-                                               group_size, lo, hi, static_cast<__nv_bfloat16*>(dW));
-  return cudaGetLastError();
 }
 
 }  // namespace awqdev
