@@ -18,12 +18,19 @@
 // feeds 512 rows of MMA work, which keeps the producer's CUDA-core cost well
 // under the tensor-core time of the same K step.
 //
+// The W tile of a K step is loaded by TMA with 128-byte swizzle straight into
+// the B operand slot, which is the tensor cores' N-major layout; each
+// producer thread reads its 16-byte chunks there and overwrites them in
+// place with the same chunks of D.  X (A operand, 4 stages) and W/D (B
+// operand, 5 stages) have separate rings; the small per-step inputs of the
+// producers (s and 1/s of the 64 rows, step / zero of the group) ride in a
+// side slot of the B ring.
+//
 // Roles (640 threads per CTA):
 //   warp 0      TMA: X subtiles (K-major, 128-byte swizzle) per K step; the
 //               completion is counted on the even CTA's barrier
 //   warp 1      TMEM allocation; in the even CTA the single-thread MMA issuer
-//   warp 2      TMA: producer inputs per K step (W tile, s and 1/s slices,
-//               step / zero of the group) into a separate ring
+//   warp 2      TMA: W tile into the B slot and the side inputs, per K step
 //   warps 4-11  epilogue: TMEM -> registers, square, column sums over the
 //               CTA's 256 rows (fixed order), one fp32 partial per column
 //   warps 12-19 producers: two groups of 4 warps on alternate K steps
@@ -44,29 +51,27 @@ constexpr int kSubRows = 128;                  // X rows of one subtile in one C
 constexpr int kStack = 2;                      // stacked subtiles per CTA
 constexpr int kPairN = 256;                    // columns of W per work unit
 constexpr int kHalfN = kPairN / 2;             // columns produced by one CTA
-constexpr int kStages = 3;                     // X / D ring
-constexpr int kWStages = 3;                    // producer-input ring
+constexpr int kAStages = 4;                    // X ring
+constexpr int kBStages = 5;                    // W -> D ring
 constexpr int kASubBytes = kSubRows * kBK * 2;  // 16 KB
 constexpr int kABytes = kStack * kASubBytes;    // 32 KB
 constexpr int kBBytes = kBK * kHalfN * 2;       // 16 KB: 64 K x 128 N bf16, N-major, 128B swizzle
-constexpr int kWTileBytes = kBK * kHalfN * 2;   // 16 KB: 64 rows x 128 columns bf16 (two 64-column boxes)
-constexpr int kSBytes = kBK * 4;                // s slice
+constexpr int kSBytes = kBK * 4;                // s slice (and 1/s slice)
 constexpr int kQBytes = (kHalfN / kQChunkCols) * kQChunkFloats * 4;  // step / zero chunks of 128 columns
-constexpr int kWStageTx = kWTileBytes + 2 * kSBytes + kQBytes;
-constexpr int kWStageStride = (kWStageTx + 127) / 128 * 128;  // TMA destinations stay 128-byte aligned
-constexpr int kOffB = kStages * kABytes;
-constexpr int kOffW = kOffB + kStages * kBBytes;
-constexpr int kSmemBytes = kOffW + kWStages * kWStageStride;
+constexpr int kSideTx = 2 * kSBytes + kQBytes;
+constexpr int kSideStride = (kSideTx + 127) / 128 * 128;  // TMA destinations stay 128-byte aligned
+constexpr int kOffB = kAStages * kABytes;
+constexpr int kOffSide = kOffB + kBStages * kBBytes;
+constexpr int kSmemBytes = kOffSide + kBStages * kSideStride;
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 640;
 constexpr int kEpiWarp0 = 4, kEpiWarps = 8;
 constexpr int kProdWarp0 = 12, kProdWarps = 8;
 constexpr int kGroupWarps = 4;                   // producer warps per K step (two groups alternate)
 static_assert(kProdWarps == 2 * kGroupWarps, "two producer groups");
-constexpr int kFullCount = 1 + 2 * kGroupWarps;  // TMA expect-tx + one producer group of each CTA
+constexpr int kBFullCount = 2 * kGroupWarps;     // one producer group of each CTA
 constexpr int kAccEmptyCount = 2 * kEpiWarps;
 
-static_assert(kWTileBytes + 2 * kSBytes + kQBytes <= kWStageStride, "W stage");
 static_assert(kSmemBytes + 1024 + 4608 <= 227 * 1024, "shared memory (dynamic + alignment slack + static)");
 
 struct FusedArgs {
@@ -102,19 +107,25 @@ __device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
 // Four rows x 8 columns of the negated difference tile D = W - S^-1 W'hat:
 //   w' = w s;  t = rint(w' / step) + zero, held as 1.5*2^23 + code;  clamp
 //   to the code range;  d = (w' - (code - zero) step) / s.
-// (D and -D give the same loss.)  `w` points at row 0 (16 bytes of 8 bf16),
-// rows 128 bytes apart; s4 / r4 hold s and 1/s of the 4 rows.
-__device__ __forceinline__ void produce4(const uint8_t* w, float4 s4, float4 r4, const float2 (&inv2)[4],
-                                         const float2 (&zm2)[4], const float2 (&nzm2)[4], const float2 (&nstep2)[4],
-                                         float lo, float hi, uint32_t (&o)[4][4]) {
+// (D and -D give the same loss.)  `w` points at the 16-byte chunk of row 0
+// in the swizzled B slot; row i's chunk sits at w + i*128 with its 16-byte
+// position XOR-ed by i (rows 4*half .. 4*half+3 of an 8-row swizzle atom).
+// Each chunk of W is overwritten in place by the same chunk of D.
+__device__ __forceinline__ void produce4(uint8_t* w, int c8, int half, float4 s4, float4 r4,
+                                         const float2 (&inv2)[4], const float2 (&zm2)[4],
+                                         const float2 (&nzm2)[4], const float2 (&nstep2)[4], float lo, float hi) {
   const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
   const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
+  uint4 wv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    wv[i] = *reinterpret_cast<const uint4*>(w + i * 128 + ((c8 ^ (4 * half + i)) * 16));
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint4 wv = *reinterpret_cast<const uint4*>(w + i * 128);
-    const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+    const uint32_t wu[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
     const float2 s2 = make_float2(sv[i], sv[i]);
     const float2 r2 = make_float2(rv[i], rv[i]);
+    uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 w2 = make_float2(bf16lo(wu[j]), bf16hi(wu[j]));
@@ -125,8 +136,9 @@ __device__ __forceinline__ void produce4(const uint8_t* w, float4 s4, float4 r4,
       const float2 qz = __fadd2_rn(tq, nzm2[j]);
       const float2 ev = __ffma2_rn(qz, nstep2[j], wp);
       const float2 d = __fmul2_rn(ev, r2);
-      o[i][j] = pack_bf16x2(d.x, d.y);
+      o[j] = pack_bf16x2(d.x, d.y);
     }
+    *reinterpret_cast<uint4*>(w + i * 128 + ((c8 ^ (4 * half + i)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -148,12 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmQ, FusedArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[kStages];    // used in the even CTA only
-  __shared__ __align__(8) uint64_t empty_bar[kStages];   // both CTAs, one arrival by the MMA commit
-  __shared__ __align__(8) uint64_t wfull_bar[kWStages];
-  __shared__ __align__(8) uint64_t wempty_bar[kWStages];
-  __shared__ __align__(8) uint64_t acc_full_bar;         // both CTAs
-  __shared__ __align__(8) uint64_t acc_empty_bar;        // even CTA
+  __shared__ __align__(8) uint64_t afull_bar[kAStages];   // even CTA: X of both CTAs landed
+  __shared__ __align__(8) uint64_t aempty_bar[kAStages];  // both CTAs: MMAs done with the X slot
+  __shared__ __align__(8) uint64_t wfull_bar[kBStages];   // local: W tile and side inputs landed
+  __shared__ __align__(8) uint64_t bfull_bar[kBStages];   // even CTA: D written by both CTAs
+  __shared__ __align__(8) uint64_t bempty_bar[kBStages];  // both CTAs: MMAs done with the B slot
+  __shared__ __align__(8) uint64_t acc_full_bar;          // both CTAs
+  __shared__ __align__(8) uint64_t acc_empty_bar;         // even CTA
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float red[4][kPairN];
@@ -167,13 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int KB = p.D_in / kBK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full_bar[s], kFullCount);
-      mbar_init(&empty_bar[s], 1);
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&afull_bar[s], 1);
+      mbar_init(&aempty_bar[s], 1);
     }
-    for (int s = 0; s < kWStages; ++s) {
+    for (int s = 0; s < kBStages; ++s) {
       mbar_init(&wfull_bar[s], 1);
-      mbar_init(&wempty_bar[s], kGroupWarps);
+      mbar_init(&bfull_bar[s], kBFullCount);
+      mbar_init(&bempty_bar[s], 1);
     }
     mbar_init(&acc_full_bar, 1);
     mbar_init(&acc_empty_bar, kAccEmptyCount);
@@ -199,7 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &abort_sh;
 
   // shared::cluster addresses of the even CTA's barriers
-  const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);
+  const uint32_t afull0 = mapa_shared(smem_u32(&afull_bar[0]), 0);
+  const uint32_t bfull0 = mapa_shared(smem_u32(&bfull_bar[0]), 0);
   const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty_bar), 0);
 
   if (warp == 0) {
@@ -210,11 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = decode_tile(t, p);
         const int row0 = tl.m_blk * (2 * kStack * kSubRows) + static_cast<int>(rank) * kSubRows;
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          if (it >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1, p.status, abort_flag)) break;
-          if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * kABytes);
-          const uint32_t bar = full0 + static_cast<uint32_t>(s) * 8u;
+          const int s = it % kAStages;
+          const uint32_t ph = (it / kAStages) & 1;
+          if (it >= kAStages && !mbar_wait_cluster(&aempty_bar[s], ph ^ 1, p.status, abort_flag)) break;
+          if (leader) mbar_arrive_expect_tx(&afull_bar[s], 2 * kABytes);
+          const uint32_t bar = afull0 + static_cast<uint32_t>(s) * 8u;
 #pragma unroll
           for (int sub = 0; sub < kStack; ++sub)
             tma_load_2d_pair(smem + s * kABytes + sub * kASubBytes, &tmX, bar, kb * kBK,
@@ -224,9 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // drain: the MMA commits of the last steps arrive on this CTA's empty
       // barriers; wait for them so that no arrival targets an exited CTA
-      const int first = it - kStages < 0 ? 0 : it - kStages;
+      const int first = it - kAStages < 0 ? 0 : it - kAStages;
       for (int j = first; j < it; ++j)
-        mbar_wait_cluster(&empty_bar[j % kStages], (j / kStages) & 1, p.status, abort_flag);
+        mbar_wait_cluster(&aempty_bar[j % kAStages], (j / kAStages) & 1, p.status, abort_flag);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer (even CTA)
@@ -239,15 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          if (!mbar_wait_cluster(&full_bar[s], ph, p.status, abort_flag)) {
+          const int sa = it % kAStages;
+          const int sb = it % kBStages;
+          if (!mbar_wait_cluster(&afull_bar[sa], (it / kAStages) & 1, p.status, abort_flag) ||
+              !mbar_wait_cluster(&bfull_bar[sb], (it / kBStages) & 1, p.status, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + s * kABytes);
-          const uint32_t b_addr = smem_u32(smem + kOffB + s * kBBytes);
+          const uint32_t a_addr = smem_u32(smem + sa * kABytes);
+          const uint32_t b_addr = smem_u32(smem + kOffB + sb * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // B: N-major SW128; 64-column chunks 8 KB apart (LBO), 8-row K
@@ -259,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_bf16_pair(tmem + static_cast<uint32_t>(sub * kPairN), ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             }
           }
-          umma_commit_pair_mc(&empty_bar[s], 0x3);
+          umma_commit_pair_mc(&aempty_bar[sa], 0x3);
+          umma_commit_pair_mc(&bempty_bar[sb], 0x3);
         }
         if (!ok) break;
         umma_commit_pair_mc(&acc_full_bar, 0x3);
@@ -268,30 +285,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tc > 0 && !*abort_flag) mbar_wait_cluster(&acc_empty_bar, (tc - 1) & 1, p.status, abort_flag);
     }
   } else if (warp == 2) {
-    // ---------------------------------------------------------- producer-input loader
+    // ---------------------------------------------------------- W / side-input loader
     if (lane == 0) {
-      int wit = 0;
+      int it = 0;
       for (int t = pair; t < p.num_tiles && !*abort_flag; t += npairs) {
         const Tile tl = decode_tile(t, p);
         const int n_base = tl.n_blk * kPairN + static_cast<int>(rank) * kHalfN;
-        for (int kb = 0; kb < KB; ++kb, ++wit) {
-          const int s = wit % kWStages;
-          const uint32_t ph = (wit / kWStages) & 1;
-          if (wit >= kWStages && !mbar_wait(&wempty_bar[s], ph ^ 1, p.status, abort_flag)) break;
-          uint8_t* st = smem + kOffW + s * kWStageStride;
-          mbar_arrive_expect_tx(&wfull_bar[s], kWStageTx);
-          tma_load_2d(st, &tmW, &wfull_bar[s], n_base, kb * kBK);
-          tma_load_2d(st + kWTileBytes / 2, &tmW, &wfull_bar[s], n_base + 64, kb * kBK);
-          tma_load_2d(st + kWTileBytes, &tmS, &wfull_bar[s], kb * kBK, tl.k);
-          tma_load_2d(st + kWTileBytes + kSBytes, &tmR, &wfull_bar[s], kb * kBK, tl.k);
-          tma_load_3d(st + kWTileBytes + 2 * kSBytes, &tmQ, &wfull_bar[s], 0, n_base / kQChunkCols,
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % kBStages;
+          const uint32_t ph = (it / kBStages) & 1;
+          if (it >= kBStages && !mbar_wait_cluster(&bempty_bar[s], ph ^ 1, p.status, abort_flag)) break;
+          uint8_t* bst = smem + kOffB + s * kBBytes;
+          uint8_t* side = smem + kOffSide + s * kSideStride;
+          mbar_arrive_expect_tx(&wfull_bar[s], kBBytes + kSideTx);
+          tma_load_2d(bst, &tmW, &wfull_bar[s], n_base, kb * kBK);
+          tma_load_2d(bst + kBBytes / 2, &tmW, &wfull_bar[s], n_base + 64, kb * kBK);
+          tma_load_2d(side, &tmS, &wfull_bar[s], kb * kBK, tl.k);
+          tma_load_2d(side + kSBytes, &tmR, &wfull_bar[s], kb * kBK, tl.k);
+          tma_load_3d(side + 2 * kSBytes, &tmQ, &wfull_bar[s], 0, n_base / kQChunkCols,
                       tl.k * p.T + (kb * kBK) / p.group_size);
         }
         if (*abort_flag) break;
       }
-      // drain loads still in flight into this CTA
-      const int first = wit - kWStages < 0 ? 0 : wit - kWStages;
-      for (int j = first; j < wit; ++j) mbar_wait(&wfull_bar[j % kWStages], (j / kWStages) & 1, nullptr, nullptr);
+      // drain: the MMA commits of the last steps arrive on this CTA's empty
+      // barriers (which also implies every load landed)
+      const int first = it - kBStages < 0 ? 0 : it - kBStages;
+      for (int j = first; j < it; ++j)
+        mbar_wait_cluster(&bempty_bar[j % kBStages], (j / kBStages) & 1, p.status, abort_flag);
     }
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
     // ---------------------------------------------------------- epilogue
@@ -351,18 +371,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb, ++it) {
         if ((it & 1) != grp_id) continue;
-        const int ws = it % kWStages;
-        if (!mbar_wait(&wfull_bar[ws], (it / kWStages) & 1, p.status, abort_flag)) {
+        const int s = it % kBStages;
+        if (!mbar_wait(&wfull_bar[s], (it / kBStages) & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
-        const int s = it % kStages;
-        const uint8_t* st = smem + kOffW + ws * kWStageStride;
+        const uint8_t* side = smem + kOffSide + s * kSideStride;
         const int grp = (kb * kBK) / p.group_size;
         if (grp != cached_group) {
           cached_group = grp;
           // chunk c: {1/step x8, 1.5*2^23 + zero x8, step x8, unused x4}
-          const float4* qp = reinterpret_cast<const float4*>(st + kWTileBytes + 2 * kSBytes + c * (kQChunkFloats * 4));
+          const float4* qp = reinterpret_cast<const float4*>(side + 2 * kSBytes + c * (kQChunkFloats * 4));
           const float4 i0 = qp[0], i1 = qp[1], z0 = qp[2], z1 = qp[3], s0 = qp[4], s1 = qp[5];
           inv2[0] = make_float2(i0.x, i0.y);
           inv2[1] = make_float2(i0.z, i0.w);
@@ -379,33 +398,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) nzm2[j] = make_float2(-zm2[j].x, -zm2[j].y);
         }
-        const uint8_t* wrow = st + h * (kWTileBytes / 2) + (rg * 8) * 128 + c8 * 16;
-        const float* srow = reinterpret_cast<const float*>(st + kWTileBytes) + rg * 8;
-        const float* rrow = reinterpret_cast<const float*>(st + kWTileBytes + kSBytes) + rg * 8;
-        uint8_t* brow = smem + kOffB + s * kBBytes + h * (kBK * 128) + (rg * 8) * 128;
+        const float* srow = reinterpret_cast<const float*>(side) + rg * 8;
+        const float* rrow = reinterpret_cast<const float*>(side + kSBytes) + rg * 8;
+        uint8_t* wrow = smem + kOffB + s * kBBytes + h * (kBK * 128) + (rg * 8) * 128;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t o[4][4];
-          produce4(wrow + half * 4 * 128, *reinterpret_cast<const float4*>(srow + half * 4),
-                   *reinterpret_cast<const float4*>(rrow + half * 4), inv2, zm2, nzm2, nstep2, lo, hi, o);
-          // the operand slot is reused once the MMAs that read it 3 steps ago completed
-          if (half == 0 && it >= kStages &&
-              !mbar_wait_cluster(&empty_bar[s], ((it / kStages) & 1) ^ 1, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = half * 4 + i;  // row within the thread's 8 (row & 7 == r)
-            *reinterpret_cast<uint4*>(brow + r * 128 + ((c8 ^ r) * 16)) = make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
-          }
-        }
-        if (!ok) break;
+        for (int half = 0; half < 2; ++half)
+          produce4(wrow + half * 4 * 128, c8, half, *reinterpret_cast<const float4*>(srow + half * 4),
+                   *reinterpret_cast<const float4*>(rrow + half * 4), inv2, zm2, nzm2, nstep2, lo, hi);
+        fence_proxy_async_smem();  // stores visible to the tensor cores
         __syncwarp();
-        if (lane == 0) mbar_arrive(&wempty_bar[ws]);  // the loader may refill this input stage
-        fence_proxy_async_smem();                     // stores visible to the tensor cores
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(full0 + static_cast<uint32_t>(s) * 8u);
+        if (lane == 0) mbar_arrive_remote(bfull0 + static_cast<uint32_t>(s) * 8u);
       }
       if (!ok) break;
     }
@@ -455,8 +457,9 @@ cudaError_t launch_search_fused(PFN_cuTensorMapEncodeTiled_v12000 encode, const 
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D_out), static_cast<cuuint64_t>(D_in)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D_out) * 2};
     const cuuint32_t box[2] = {64, kBK};
+    // 128-byte swizzle: the tile lands in the tensor cores' N-major B layout
     e = encode_map(encode, &tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dims, strides, box,
-                   CU_TENSOR_MAP_SWIZZLE_NONE);
+                   CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
   }
   {
