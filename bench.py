@@ -3,7 +3,8 @@
 
 One step = the whole path on one synthetic layer whose inputs are resident in
 HBM: act_stats (mean |X|) -> search (21-point alpha grid, candidate losses,
-argmin, s*) -> quantize_pack (int4 codes, fp16 scales / zeros).
+argmin, s*) -> quantize_pack_searched (int4 codes, fp16 scales / zeros, with
+the group parameters the search computed for alpha*).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload attn_proj]
@@ -28,7 +29,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "AWQ alpha-search TFLOP/s & layers/sec (21-pt grid) vs tensor-pipe peak; pack GB/s"
 KERNELS_PER_LAUNCHER = {"act_stats": 1, "scale_table": 1, "group_params": 1, "search_fused": 1,
-                        "reduce_argmin": 1, "pack": 1}
+                        "reduce_argmin": 1, "pack": 1, "pack_searched": 1}
 SEARCH_KERNELS = ("search_fused",)
 
 
@@ -236,7 +237,9 @@ def workload_bytes(w, G):
     N, Di, Do, g = w.N, w.D_in, w.D_out, w.group_size
     flops = 2.0 * N * Di * Do * G
     stats_bytes = 2.0 * N * Di + 4.0 * Di
-    pack_bytes = 2.0 * Di * Do + 4.0 * Di + Di * Do / 2.0 + 4.0 * Do * Di / g
+    # the searched pack reads W, s and the best candidate's step, 1/step and
+    # zero (12 bytes per group and column); writes codes, fp16 scales and zeros
+    pack_bytes = 2.0 * Di * Do + 4.0 * Di + Di * Do / 2.0 + 4.0 * Do * Di / g + 12.0 * Do * Di / g
     return flops, stats_bytes, pack_bytes
 
 
@@ -346,7 +349,6 @@ def run_ours(args, world, rank, local):
     a_buf = torch.empty(Di, dtype=torch.float32, device=dev)
     ws_s = torch.empty(awq.act_stats_workspace_size(N, Di), dtype=torch.uint8, device=dev)
     ws_q = torch.empty(awq.search_workspace_size(N, Di, Do, G, g, sym), dtype=torch.uint8, device=dev)
-    ws_p = torch.empty(256, dtype=torch.uint8, device=dev)
     res = awq.SearchResult(torch.empty(G, dtype=torch.float64, device=dev), torch.empty(1, dtype=torch.int32, device=dev),
                            torch.empty(Di, dtype=torch.float32, device=dev), None, grid, ws_q)
     pk = (torch.empty(Di // 2, Do, dtype=torch.uint8, device=dev), torch.empty(T, Do, dtype=torch.float16, device=dev),
@@ -356,12 +358,12 @@ def run_ours(args, world, rank, local):
     def step(Xs, Ws):
         awq.act_stats(Xs, out=a_buf, ws=ws_s, check=False)
         awq.search(Xs, Ws, a_buf, grid, g, sym, ws=ws_q, out=res, check=False)
-        awq.quantize_pack(Ws, res.s_star, g, sym, out=pk, ws=ws_p, check=False)
+        awq.quantize_pack_searched(Ws, res, g, sym, out=pk)
 
     for _ in range(args.warmup):
         flush.zero_()
         step(Xd, Wd)
-    for ws, nm in ((ws_s, "act_stats"), (ws_q, "search"), (ws_p, "pack")):
+    for ws, nm in ((ws_s, "act_stats"), (ws_q, "search")):
         awq.check_workspace(ws, nm)
     torch.cuda.synchronize()
 
@@ -393,7 +395,7 @@ def run_ours(args, world, rank, local):
 
     search_name = next((k for k in SEARCH_KERNELS if k in kern), "search_fused")
     gemm_ms = per_launch_ms(search_name)
-    pack_ms = per_launch_ms("pack")
+    pack_ms = per_launch_ms("pack_searched")
     stats_ms = per_launch_ms("act_stats")
     peaks, peak_src = measured_peaks()
     achieved = flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
@@ -437,7 +439,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
     e2e_ms = max_over_ranks(e2e_ms, world)
-    for ws, nm in ((ws_s, "act_stats"), (ws_q, "search"), (ws_p, "pack")):
+    for ws, nm in ((ws_s, "act_stats"), (ws_q, "search")):
         awq.check_workspace(ws, nm)
 
     line = {

@@ -193,6 +193,32 @@ AWQ_API awq_status awq_quantize_pack(const void* W, const float* s, int64_t D_in
                              const awq_cfg* cfg, uint8_t* qweight, void* scales, void* zeros,
                              void* ws, size_t ws_bytes, awq_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Step 4 right after a search: the same packing, with the per-group
+ * quantiser parameters the search already computed for its best candidate.
+ *
+ * awq_search evaluates every candidate with the pack's own quantiser (adr
+ * "009. AWQ Integration", 关键设计 3: search and pack share one quantiser), so
+ * its workspace already holds, for alpha*, the exact step (fp16-rounded) and
+ * zero of every (group, column) that awq_quantize_pack would compute from
+ * diag(s*) W.  This call reads them instead of recomputing them and packs in
+ * one streaming pass over W.
+ *
+ *   W, D_in, D_out, cfg    the same W and cfg as the awq_search call
+ *   G                      that call's grid size
+ *   search_ws, search_ws_bytes  that call's workspace, unchanged since
+ *   best_idx, s_star       that call's device outputs (s_star 16-byte aligned)
+ *   qweight, scales, zeros as for awq_quantize_pack (scales, zeros 16-byte aligned)
+ * The outputs equal awq_quantize_pack(W, s_star, ...) bit for bit.  Device
+ * errors of W (non-finite values, fp16 step overflow) were already reported
+ * in the search workspace's status word; this call adds none.  Must be
+ * ordered after the search on the device (same stream, or an event).
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_quantize_pack_searched(const void* W, int64_t D_in, int64_t D_out, int32_t G,
+                                              const awq_cfg* cfg, const void* search_ws, size_t search_ws_bytes,
+                                              const int32_t* best_idx, const float* s_star, uint8_t* qweight,
+                                              void* scales, void* zeros, awq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

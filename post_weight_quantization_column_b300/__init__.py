@@ -9,6 +9,7 @@ the library is missing or the device is not sm_103 the calls raise.
     a = act_stats(X)                                  # mean |X[:, j]|
     r = search(X, W, a)                               # alpha grid search
     qweight, scales, zeros = quantize_pack(W, r.s_star)
+    qweight, scales, zeros = quantize_pack_searched(W, r)   # same, reusing the search's parameters
 """
 from __future__ import annotations
 
@@ -59,6 +60,8 @@ _SIGS = {
     "awq_pack_workspace_size": ([_c_i64, _c_i64, ctypes.POINTER(awq_cfg), ctypes.POINTER(_c_sz)], ctypes.c_int),
     "awq_quantize_pack": ([_vp, _vp, _c_i64, _c_i64, ctypes.POINTER(awq_cfg), _vp, _vp, _vp, _vp, _c_sz, _vp],
                           ctypes.c_int),
+    "awq_quantize_pack_searched": ([_vp, _c_i64, _c_i64, _c_i32, ctypes.POINTER(awq_cfg), _vp, _c_sz, _vp, _vp,
+                                    _vp, _vp, _vp, _vp], ctypes.c_int),
     "awq_selftest_gemm_bf16": ([_vp, _vp, _c_i32, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_sz, _vp], ctypes.c_int),
     "awq_profile_enable": ([_c_i32], ctypes.c_int),
     "awq_profile_collect": ([ctypes.POINTER(awq_kernel_time), _c_i32, ctypes.POINTER(_c_i32)], ctypes.c_int),
@@ -240,6 +243,30 @@ def quantize_pack(W: torch.Tensor, s: torch.Tensor, group_size: int = 128, symme
            "awq_quantize_pack")
     if check:
         check_workspace(ws, "awq_quantize_pack (device)", stream)
+    return qweight, scales, zeros
+
+
+def quantize_pack_searched(W: torch.Tensor, result: SearchResult, group_size: int = 128, symmetric: bool = False,
+                           out=None, stream=None):
+    """The pack right after `search`: same outputs as quantize_pack(W, result.s_star), using the group
+    parameters the search computed for its best candidate (one streaming pass over W)."""
+    _need(W, torch.bfloat16, "W")
+    D_in, D_out = W.shape
+    dev = W.device
+    if D_in % group_size:
+        raise ValueError("D_in must be a multiple of group_size")
+    T = D_in // group_size
+    if out is None:
+        out = (torch.empty(D_in // 2, D_out, dtype=torch.uint8, device=dev),
+               torch.empty(T, D_out, dtype=torch.float16, device=dev),
+               torch.empty(T, D_out, dtype=torch.float16, device=dev))
+    qweight, scales, zeros = out
+    cfg = make_cfg(group_size, symmetric)
+    ws = result.workspace
+    _check(lib().awq_quantize_pack_searched(_ptr(W), D_in, D_out, len(result.grid), ctypes.byref(cfg), _ptr(ws),
+                                            ws.numel(), _ptr(result.best_idx), _ptr(result.s_star), _ptr(qweight),
+                                            _ptr(scales), _ptr(zeros), _stream_handle(stream)),
+           "awq_quantize_pack_searched")
     return qweight, scales, zeros
 
 

@@ -183,6 +183,14 @@ SearchLayout search_layout(int64_t N, int64_t D_in, int64_t D_out, int G, int gr
   return L;
 }
 
+// Offset of the group-parameter table inside a search workspace (the layout
+// before it depends only on D_in and G).
+size_t search_qp_offset(int64_t D_in, int G) {
+  const size_t g = static_cast<size_t>(G), din = static_cast<size_t>(D_in);
+  size_t off = align_up(kHeaderBytes + g * din * 4, 256);
+  return align_up(off + g * din * 4, 256);
+}
+
 awq_status validate_search_shape(int64_t N, int64_t D_in, int64_t D_out, int32_t G, const awq_cfg* cfg) {
   awq_status st = validate_cfg(cfg);
   if (st != AWQ_OK) return st;
@@ -364,6 +372,31 @@ awq_status awq_quantize_pack(const void* W, const float* s, int64_t D_in, int64_
   ProfScope prof("pack", cs);
   return from_cuda(launch_pack(encode, W, s, D_in, D_out, cfg->group_size, cfg->symmetric, qweight, scales, zeros,
                                status_word(ws), sms, cs));
+}
+
+awq_status awq_quantize_pack_searched(const void* W, int64_t D_in, int64_t D_out, int32_t G, const awq_cfg* cfg,
+                                      const void* search_ws, size_t search_ws_bytes, const int32_t* best_idx,
+                                      const float* s_star, uint8_t* qweight, void* scales, void* zeros,
+                                      awq_stream_t stream) {
+  awq_status st = validate_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (G < 1 || G > kMaxGrid) return AWQ_ERR_SHAPE;
+  if (D_in < 0 || D_out < 0) return AWQ_ERR_SHAPE;
+  if (D_in % cfg->group_size != 0 || D_out % 8 != 0) return AWQ_ERR_SHAPE;
+  if (D_in == 0 || D_out == 0) return AWQ_OK;
+  if (!W || !search_ws || !best_idx || !s_star || !qweight || !scales || !zeros) return AWQ_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(search_ws, 256) || !aligned(best_idx, 4) || !aligned(s_star, 16) ||
+      !aligned(qweight, 8) || !aligned(scales, 16) || !aligned(zeros, 16))
+    return AWQ_ERR_ALIGNMENT;
+  const size_t qp_off = search_qp_offset(D_in, G);
+  if (search_ws_bytes < qp_off + qparam_floats(G, D_in / cfg->group_size, D_out) * 4) return AWQ_ERR_WORKSPACE;
+  st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const float* qp = reinterpret_cast<const float*>(static_cast<const uint8_t*>(search_ws) + qp_off);
+  ProfScope prof("pack_searched", cs);
+  return from_cuda(launch_pack_searched(W, s_star, qp, best_idx, D_in, D_out, cfg->group_size, cfg->symmetric,
+                                        qweight, scales, zeros, cs));
 }
 
 // ------------------------------------------------------------------ self-test GEMM

@@ -54,6 +54,11 @@ cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in,
 cudaError_t launch_pack(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* W, const float* s, int64_t D_in,
                         int64_t D_out, int group_size, int symmetric, uint8_t* qweight, void* scales, void* zeros,
                         uint32_t* status, int num_sms, cudaStream_t stream);
+// Pack with the group parameters a search computed for its best candidate
+// (qp: the search workspace's parameter table, best_idx: device int32).
+cudaError_t launch_pack_searched(const void* W, const float* s, const float* qp, const int32_t* best_idx, int64_t D_in,
+                                 int64_t D_out, int group_size, int symmetric, uint8_t* qweight, void* scales,
+                                 void* zeros, cudaStream_t stream);
 
 // ----------------------------------------------------------------- tensor-core self-test
 constexpr int kGemmBM = 128;

@@ -414,6 +414,181 @@ cudaError_t launch_pack_g(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* 
   return launch_pack_t<GS, false>(encode, W, s, D_in, D_out, qweight, scales, zeros, status, num_sms, stream);
 }
 
+
+// ---------------------------------------------------------------------------
+// Pack after a search.  The search's group-parameter pass already holds, for
+// every candidate, the exact step (fp16-rounded range / 15 or max|w'| / 7),
+// 1/step and zero of every (group, column) -- the same formulas and the same
+// exact ranges as pass 1 above.  For its best candidate the pack is then a
+// single streaming pass: thread t of the grid owns 8 columns (chunk c) x 8
+// rows of one group, loads all 8 rows at once, and emits codes exactly as
+// pass 2 above (with the same exact-division redo near ties); the threads
+// of chunk-0-row-block write the group's fp16 scales and zeros.
+constexpr int kSearchedRows = 8;
+constexpr int kSearchedThreads = 256;
+
+// The exact path of one thread's 8 rows x 8 columns (rare: only where some
+// quotient lies within the tie guard of a half step): codes from the IEEE
+// fp32 quotient w'/step, as the oracle defines them.  Kept out of line so
+// that its registers do not burden the streaming path.
+template <bool SYM>
+__device__ __noinline__ void pack_searched_exact(const __nv_bfloat16* __restrict__ W, const float* __restrict__ s,
+                                                 const float* __restrict__ qc, int64_t row0, int64_t n,
+                                                 int64_t D_out, uint8_t* __restrict__ qweight) {
+  for (int p = 0; p < kSearchedRows / 2; ++p) {
+    const uint4 a = *reinterpret_cast<const uint4*>(W + (row0 + 2 * p) * D_out + n);
+    const uint4 b = *reinterpret_cast<const uint4*>(W + (row0 + 2 * p + 1) * D_out + n);
+    const float se = s[row0 + 2 * p], so = s[row0 + 2 * p + 1];
+    const uint32_t we[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t wo[4] = {b.x, b.y, b.z, b.w};
+    uint32_t bytes[8];
+    for (int j = 0; j < 8; ++j) {
+      const float xe = (j & 1) ? bf16hi(we[j >> 1]) : bf16lo(we[j >> 1]);
+      const float xo = (j & 1) ? bf16hi(wo[j >> 1]) : bf16lo(wo[j >> 1]);
+      const float step = qc[2 * kQChunkCols + j];
+      const float zo = SYM ? 8.f : qc[kQChunkCols + j] - kMagic;
+      const float ql = SYM ? 1.f : 0.f;
+      // clamp(rint(IEEE w'/step) + zero, ql, 15); a zero step keeps the zero
+      uint32_t ke = static_cast<uint32_t>(zo), ko = ke;
+      if (step != 0.f) {
+        const float qe = rintf(__fdiv_rn(__fmul_rn(xe, se), step)) + zo;
+        const float qo = rintf(__fdiv_rn(__fmul_rn(xo, so), step)) + zo;
+        ke = static_cast<uint32_t>(fminf(fmaxf(qe, ql), 15.f));
+        ko = static_cast<uint32_t>(fminf(fmaxf(qo, ql), 15.f));
+      }
+      bytes[j] = ke | (ko << 4);
+    }
+    *reinterpret_cast<uint2*>(qweight + (row0 / 2 + p) * D_out + n) =
+        make_uint2(bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24),
+                   bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24));
+  }
+}
+
+template <int GS, bool SYM>
+__global__ void __launch_bounds__(kSearchedThreads, 3)
+    pack_searched_kernel(const __nv_bfloat16* __restrict__ W, const float* __restrict__ s,
+                         const float* __restrict__ qp, const int32_t* __restrict__ best_idx, int64_t D_in,
+                         int64_t D_out, uint8_t* __restrict__ qweight, __half* __restrict__ scales,
+                         __half* __restrict__ zeros) {
+  constexpr int RB = GS / kSearchedRows;  // row blocks per group
+  const int64_t chunks = D_out / kQChunkCols;
+  const int64_t T = D_in / GS;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * kSearchedThreads + threadIdx.x;
+  if (idx >= T * RB * chunks) return;
+  const int64_t c = idx % chunks;  // chunk fastest: a warp reads 512 contiguous bytes per row
+  const int64_t rest = idx / chunks;
+  const int rb = static_cast<int>(rest % RB);
+  const int64_t g = rest / RB;
+  const int64_t n = c * kQChunkCols;
+  const int64_t row0 = g * GS + rb * kSearchedRows;
+
+  uint4 w[kSearchedRows];
+#pragma unroll
+  for (int i = 0; i < kSearchedRows; ++i) w[i] = *reinterpret_cast<const uint4*>(W + (row0 + i) * D_out + n);
+  float sj[kSearchedRows];
+#pragma unroll
+  for (int i = 0; i < kSearchedRows; i += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(s + row0 + i);  // rows of a group: 16-byte aligned
+    sj[i] = v.x;
+    sj[i + 1] = v.y;
+    sj[i + 2] = v.z;
+    sj[i + 3] = v.w;
+  }
+  // {1/step x8, 1.5*2^23 + zero x8, step x8} of (best candidate, group, chunk)
+  const int k = *best_idx;
+  const float* qc = qp + ((static_cast<int64_t>(k) * T + g) * chunks + c) * kQChunkFloats;
+  const float4* q4 = reinterpret_cast<const float4*>(qc);
+  float inv[8], zmz[8];  // zmz: 1.5*2^23 + the stored offset (the zero; 8 for symmetric codes)
+  {
+    const float4 i0 = q4[0], i1 = q4[1];
+    const float ia[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) inv[j] = ia[j];
+    if (SYM) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) zmz[j] = kMagic + 8.f;
+    } else {
+      const float4 z0 = q4[2], z1 = q4[3];
+      const float za[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) zmz[j] = za[j];
+    }
+  }
+  if (rb == 0) {
+    const float4 s0 = q4[4], s1 = q4[5];
+    const float st[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    uint32_t sc[4], zr[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 hs = __floats2half2_rn(st[2 * j], st[2 * j + 1]);
+      const __half2 hz = __floats2half2_rn(zmz[2 * j] - kMagic, zmz[2 * j + 1] - kMagic);
+      sc[j] = *reinterpret_cast<const uint32_t*>(&hs);
+      zr[j] = *reinterpret_cast<const uint32_t*>(&hz);
+    }
+    *reinterpret_cast<uint4*>(scales + g * D_out + n) = make_uint4(sc[0], sc[1], sc[2], sc[3]);
+    *reinterpret_cast<uint4*>(zeros + g * D_out + n) = make_uint4(zr[0], zr[1], zr[2], zr[3]);
+  }
+  const float clo = SYM ? kMagic + 1.f : kMagic;
+  const float chi = kMagic + 15.f;
+  uint32_t out[kSearchedRows / 2][2];
+  float tmax = 0.f;
+#pragma unroll
+  for (int p = 0; p < kSearchedRows / 2; ++p) {
+    const uint32_t we[4] = {w[2 * p].x, w[2 * p].y, w[2 * p].z, w[2 * p].w};
+    const uint32_t wo[4] = {w[2 * p + 1].x, w[2 * p + 1].y, w[2 * p + 1].z, w[2 * p + 1].w};
+    uint32_t half16[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 inv2 = make_float2(inv[2 * j], inv[2 * j + 1]);
+      const float2 ninv2 = make_float2(-inv[2 * j], -inv[2 * j + 1]);
+      const float2 zm2 = make_float2(zmz[2 * j], zmz[2 * j + 1]);
+      const float2 nzm2 = make_float2(-zmz[2 * j], -zmz[2 * j + 1]);
+      const float2 pe = __fmul2_rn(make_float2(bf16lo(we[j]), bf16hi(we[j])), make_float2(sj[2 * p], sj[2 * p]));
+      const float2 po = __fmul2_rn(make_float2(bf16lo(wo[j]), bf16hi(wo[j])), make_float2(sj[2 * p + 1], sj[2 * p + 1]));
+      float2 ce = __ffma2_rn(pe, inv2, zm2);
+      float2 co = __ffma2_rn(po, inv2, zm2);
+      const float2 de = __ffma2_rn(pe, ninv2, __fadd2_rn(ce, nzm2));
+      const float2 dd = __ffma2_rn(po, ninv2, __fadd2_rn(co, nzm2));
+      tmax = maxabs3(tmax, de.x, de.y);
+      tmax = maxabs3(tmax, dd.x, dd.y);
+      if (SYM) {
+        ce.x = fmaxf(ce.x, clo);
+        ce.y = fmaxf(ce.y, clo);
+        co.x = fmaxf(co.x, clo);
+        co.y = fmaxf(co.y, clo);
+      }
+      ce.x = fminf(ce.x, chi);
+      ce.y = fminf(ce.y, chi);
+      co.x = fminf(co.x, chi);
+      co.y = fminf(co.y, chi);
+      const uint32_t x0 = __float_as_uint(co.x) * 16u + __float_as_uint(ce.x);
+      const uint32_t x1 = __float_as_uint(co.y) * 16u + __float_as_uint(ce.y);
+      half16[j] = __byte_perm(x0, x1, 0x0040);
+    }
+    out[p][0] = __byte_perm(half16[0], half16[1], 0x5410);
+    out[p][1] = __byte_perm(half16[2], half16[3], 0x5410);
+  }
+  if (tmax > kTieGuard) {
+    pack_searched_exact<SYM>(W, s, qc, row0, n, D_out, qweight);
+    return;
+  }
+#pragma unroll
+  for (int p = 0; p < kSearchedRows / 2; ++p)
+    *reinterpret_cast<uint2*>(qweight + (row0 / 2 + p) * D_out + n) = make_uint2(out[p][0], out[p][1]);
+}
+
+template <int GS, bool SYM>
+cudaError_t launch_pack_searched_t(const void* W, const float* s, const float* qp, const int32_t* best_idx,
+                                   int64_t D_in, int64_t D_out, uint8_t* qweight, void* scales, void* zeros,
+                                   cudaStream_t stream) {
+  const int64_t threads = (D_in / GS) * (GS / kSearchedRows) * (D_out / kQChunkCols);
+  const int64_t blocks = (threads + kSearchedThreads - 1) / kSearchedThreads;
+  pack_searched_kernel<GS, SYM><<<static_cast<unsigned>(blocks), kSearchedThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(W), s, qp, best_idx, D_in, D_out, qweight, static_cast<__half*>(scales),
+      static_cast<__half*>(zeros));
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_pack(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* W, const float* s, int64_t D_in,
@@ -429,6 +604,27 @@ cudaError_t launch_pack(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* W,
     default:
       return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_pack_searched(const void* W, const float* s, const float* qp, const int32_t* best_idx, int64_t D_in,
+                                 int64_t D_out, int group_size, int symmetric, uint8_t* qweight, void* scales,
+                                 void* zeros, cudaStream_t stream) {
+#define AWQ_PACK_SEARCHED(GS)                                                                                   \
+  return symmetric ? launch_pack_searched_t<GS, true>(W, s, qp, best_idx, D_in, D_out, qweight, scales, zeros,   \
+                                                      stream)                                                  \
+                   : launch_pack_searched_t<GS, false>(W, s, qp, best_idx, D_in, D_out, qweight, scales, zeros, \
+                                                       stream)
+  switch (group_size) {
+    case 64:
+      AWQ_PACK_SEARCHED(64);
+    case 128:
+      AWQ_PACK_SEARCHED(128);
+    case 256:
+      AWQ_PACK_SEARCHED(256);
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef AWQ_PACK_SEARCHED
 }
 
 }  // namespace awqdev

@@ -142,3 +142,32 @@ def test_rejects_wrong_dtype(awq):
     X = torch.zeros(8, 128, device="cuda", dtype=torch.float32)
     with pytest.raises(TypeError):
         awq.act_stats(X)
+
+
+def test_pack_searched_degenerate_groups_and_ties(awq):
+    """The searched pack on zero groups, one-signed groups and weights exactly
+    on half steps (|x| = 1 everywhere, so s = 1 for every alpha)."""
+    rng = np.random.default_rng(9)
+    D_in, D_out = 256, 264
+    for sym in (False, True):
+        Xf = np.where(rng.random((64, D_in)) < 0.5, -1.0, 1.0).astype(np.float32)
+        half = np.where(rng.random((D_in, D_out)) < 0.5, 0.5, 0.0)
+        codes = rng.integers(-6, 7, size=(D_in, D_out)).astype(np.float64)
+        Wf = ((codes + half) / 64.0).astype(np.float32)
+        Wf[0, :] = 7.0 / 64.0
+        if not sym:
+            Wf[1, :] = -8.0 / 64.0
+        Wf[128:256, 0:8] = 0.0                             # zero group
+        Wf[128:256, 8:16] = np.abs(Wf[128:256, 8:16])      # one-signed groups
+        Xb, Wb = synth.to_bf16(Xf), synth.to_bf16(Wf)
+        Wf = synth.bf16_to_f32(Wb)
+        a = awq.act_stats(Xb.cuda())
+        assert torch.all(a == 1.0)
+        res = awq.search(Xb.cuda(), Wb.cuda(), a, symmetric=sym)
+        qw, sc, z = awq.quantize_pack_searched(Wb.cuda(), res, 128, sym)
+        s_star = res.s_star.cpu().numpy()
+        assert np.all(s_star == 1.0)
+        oq, osc, oz = orc.pack(Wf, s_star, 128, sym)
+        assert np.array_equal(qw.cpu().numpy(), oq)
+        assert np.array_equal(sc.cpu().numpy().view(np.uint16), osc.view(np.uint16))
+        assert np.array_equal(z.cpu().numpy().view(np.uint16), oz.view(np.uint16))

@@ -163,3 +163,35 @@ def test_search_full_size_sampled_columns(awq, name):
     assert np.array_equal(res.s_star.cpu().numpy(), orc.scales(a, grid[res.best]))
     # the sample's own argmin agrees with the oracle's on that sample
     check_alpha_star(int(np.argmin(got.sum(axis=1))), ref["losses"])
+
+
+# ---------------------------------------------------------------------------- step 4 after a search
+def _searched_pack_check(awq, w, X, W, Xf, Wf):
+    """awq_quantize_pack_searched equals the oracle's pack at the search's s*
+    (and the standalone GPU pack) bit for bit."""
+    Xd, Wd = X.cuda(), W.cuda()
+    a = awq.act_stats(Xd)
+    res = awq.search(Xd, Wd, a, group_size=w.group_size, symmetric=w.symmetric)
+    qw, sc, z = awq.quantize_pack_searched(Wd, res, w.group_size, w.symmetric)
+    s_star = res.s_star.cpu().numpy()
+    torch.cuda.synchronize()
+    oq, osc, oz = orc.pack(Wf, s_star, group_size=w.group_size, symmetric=w.symmetric)
+    assert np.array_equal(sc.cpu().numpy().view(np.uint16), osc.view(np.uint16)), "scales differ"
+    assert np.array_equal(z.cpu().numpy().view(np.uint16), oz.view(np.uint16)), "zeros differ"
+    bad = np.count_nonzero(qw.cpu().numpy() != oq)
+    assert bad == 0, f"{bad} packed bytes differ"
+    q2, s2, z2 = awq.quantize_pack(Wd, res.s_star, w.group_size, w.symmetric)
+    assert torch.equal(q2, qw) and torch.equal(s2, sc) and torch.equal(z2, z)
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_pack_searched_bit_exact(awq, name):
+    w, X, W, Xf, Wf = workload_cpu(name)
+    _searched_pack_check(awq, w, X, W, Xf, Wf)
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("w", RAGGED, ids=[r.name for r in RAGGED])
+def test_pack_searched_bit_exact_ragged(awq, w):
+    _, X, W, Xf, Wf = custom_cpu(w)
+    _searched_pack_check(awq, w, X, W, Xf, Wf)
