@@ -204,6 +204,10 @@ awq_status validate_search_shape(int64_t N, int64_t D_in, int64_t D_out, int32_t
 
 }  // namespace
 
+namespace awqdev {
+awq_status tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) { return get_encode(fn); }
+}  // namespace awqdev
+
 extern "C" {
 
 const char* awq_status_string(awq_status s) {
@@ -245,10 +249,13 @@ awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t ldx, fl
   if (N < 1 || D_in < 0) return AWQ_ERR_SHAPE;
   if (D_in == 0) return AWQ_OK;
   if (!X || !mean_abs || !ws) return AWQ_ERR_INVALID_ARG;
-  if (ldx < D_in || D_in % 8 != 0 || ldx % 8 != 0) return AWQ_ERR_SHAPE;
+  if (ldx < D_in || D_in % 8 != 0 || ldx % 8 != 0 || N > INT32_MAX || D_in > INT32_MAX) return AWQ_ERR_SHAPE;
   if (!aligned(X, 16) || !aligned(mean_abs, 4) || !aligned(ws, 256)) return AWQ_ERR_ALIGNMENT;
   if (ws_bytes < stats_ws_bytes(N, D_in)) return AWQ_ERR_WORKSPACE;
   awq_status st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  st = get_encode(&encode);
   if (st != AWQ_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int splits = 1;
@@ -260,7 +267,8 @@ awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t ldx, fl
   unsigned int* tickets = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
   float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kHeaderBytes + tb);
   ProfScope prof("act_stats", s);
-  return from_cuda(launch_act_stats(X, N, D_in, ldx, mean_abs, partial, tickets, splits, rps, status_word(ws), s));
+  return from_cuda(
+      launch_act_stats(encode, X, N, D_in, ldx, mean_abs, partial, tickets, splits, rps, status_word(ws), s));
 }
 
 // ------------------------------------------------------------------ search
@@ -395,7 +403,7 @@ awq_status awq_quantize_pack_searched(const void* W, int64_t D_in, int64_t D_out
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const float* qp = reinterpret_cast<const float*>(static_cast<const uint8_t*>(search_ws) + qp_off);
   ProfScope prof("pack_searched", cs);
-  return from_cuda(launch_pack_searched(W, s_star, qp, best_idx, D_in, D_out, cfg->group_size, cfg->symmetric,
+  return from_cuda(launch_pack_searched(W, s_star, qp, best_idx, G, D_in, D_out, cfg->group_size, cfg->symmetric,
                                         qweight, scales, zeros, cs));
 }
 

@@ -49,11 +49,14 @@ extern "C" awq_status awq_act_stats_noalloc(const void* X, int64_t N, int64_t D_
   if (D_in == 0) return AWQ_OK;
   if (D_in > kNoAllocScratchFloats) return AWQ_ERR_SHAPE;
   if (!X || !mean_abs) return AWQ_ERR_INVALID_ARG;
-  if (ldx < D_in || D_in % 8 != 0 || ldx % 8 != 0) return AWQ_ERR_SHAPE;
+  if (ldx < D_in || D_in % 8 != 0 || ldx % 8 != 0 || N > INT32_MAX) return AWQ_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(X) % 16) != 0 || (reinterpret_cast<uintptr_t>(mean_abs) % 4) != 0)
     return AWQ_ERR_ALIGNMENT;
   float* scratch = nullptr;
   awq_status st = scratch_for_current_device(&scratch);
+  if (st != AWQ_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  st = awqdev::tensor_map_encoder(&encode);
   if (st != AWQ_OK) return st;
 
   // Same row-slice plan as awq_act_stats, so both entry points sum in the same
@@ -65,7 +68,7 @@ extern "C" awq_status awq_act_stats_noalloc(const void* X, int64_t N, int64_t D_
   if (static_cast<int64_t>(splits) * D_in > kNoAllocScratchFloats) {
     const int64_t max_splits = kNoAllocScratchFloats / D_in;
     rps = (N + max_splits - 1) / max_splits;
-    rps = (rps + awqdev::kStatsRowLanes - 1) / awqdev::kStatsRowLanes * awqdev::kStatsRowLanes;
+    rps = (rps + awqdev::kStatsBoxRows - 1) / awqdev::kStatsBoxRows * awqdev::kStatsBoxRows;
     splits = static_cast<int>((N + rps - 1) / rps);
   }
   // Every partial the final sums read is rewritten by this call; the ticket
@@ -77,7 +80,7 @@ extern "C" awq_status awq_act_stats_noalloc(const void* X, int64_t N, int64_t D_
   const int64_t chunks = awqdev::stats_chunks(D_in);
   if (cudaMemsetAsync(tickets, 0, static_cast<size_t>(chunks) * sizeof(unsigned int), s) != cudaSuccess)
     return AWQ_ERR_CUDA;
-  const cudaError_t e = awqdev::launch_act_stats(X, N, D_in, ldx, mean_abs, scratch + kNoAllocTicketWords, tickets,
-                                                 splits, rps, nullptr, s);
+  const cudaError_t e = awqdev::launch_act_stats(encode, X, N, D_in, ldx, mean_abs, scratch + kNoAllocTicketWords,
+                                                 tickets, splits, rps, nullptr, s);
   return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
 }

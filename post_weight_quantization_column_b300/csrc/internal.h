@@ -11,10 +11,12 @@
 namespace awqdev {
 
 // ----------------------------------------------------------------- stats
-constexpr int kStatsThreads = 256;
-constexpr int kStatsRowLanes = 8;      // warps per CTA, each on its own rows
+constexpr int kStatsRowLanes = 8;      // consumer warps per CTA, each on its own rows of a box
+constexpr int kStatsThreads = (kStatsRowLanes + 1) * 32;  // + one producer warp
 constexpr int kStatsCols = 256;        // channels per CTA (32 lanes x 8)
-constexpr int kStatsTargetCtas = 148 * 4;
+constexpr int kStatsBoxRows = 32;      // rows per ring stage (one bulk copy per row)
+constexpr int kStatsStages = 4;        // ring depth: 4 x 16 KB
+constexpr int kStatsTargetCtas = 148 * 3;  // three CTAs (3 x 73 KB shared memory) fit on an SM
 constexpr int kStatsMaxSplits = 1024;
 
 void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split);
@@ -22,9 +24,11 @@ void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split);
 int64_t stats_chunks(int64_t D);
 // partial: fp32 [splits][D] scratch; tickets: uint32 [stats_chunks(D)], zero on
 // entry (the kernel leaves them zero again).
-cudaError_t launch_act_stats(const void* X, int64_t N, int64_t D, int64_t ldx, float* mean_abs, float* partial,
-                             unsigned int* tickets, int splits, int64_t rows_per_split, uint32_t* status,
-                             cudaStream_t stream);
+cudaError_t launch_act_stats(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, int64_t N, int64_t D,
+                             int64_t ldx, float* mean_abs, float* partial, unsigned int* tickets, int splits,
+                             int64_t rows_per_split, uint32_t* status, cudaStream_t stream);
+// The driver's tensor-map encoder (resolved once per process).
+awq_status tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn);
 
 // ----------------------------------------------------------------- quantiser
 constexpr int kMaxGrid = 64;
@@ -56,9 +60,9 @@ cudaError_t launch_pack(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* W,
                         uint32_t* status, int num_sms, cudaStream_t stream);
 // Pack with the group parameters a search computed for its best candidate
 // (qp: the search workspace's parameter table, best_idx: device int32).
-cudaError_t launch_pack_searched(const void* W, const float* s, const float* qp, const int32_t* best_idx, int64_t D_in,
-                                 int64_t D_out, int group_size, int symmetric, uint8_t* qweight, void* scales,
-                                 void* zeros, cudaStream_t stream);
+cudaError_t launch_pack_searched(const void* W, const float* s, const float* qp, const int32_t* best_idx, int G,
+                                 int64_t D_in, int64_t D_out, int group_size, int symmetric, uint8_t* qweight,
+                                 void* scales, void* zeros, cudaStream_t stream);
 
 // ----------------------------------------------------------------- tensor-core self-test
 constexpr int kGemmBM = 128;

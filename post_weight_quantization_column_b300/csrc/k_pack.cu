@@ -467,7 +467,7 @@ __device__ __noinline__ void pack_searched_exact(const __nv_bfloat16* __restrict
 template <int GS, bool SYM>
 __global__ void __launch_bounds__(kSearchedThreads, 3)
     pack_searched_kernel(const __nv_bfloat16* __restrict__ W, const float* __restrict__ s,
-                         const float* __restrict__ qp, const int32_t* __restrict__ best_idx, int64_t D_in,
+                         const float* __restrict__ qp, const int32_t* __restrict__ best_idx, int G, int64_t D_in,
                          int64_t D_out, uint8_t* __restrict__ qweight, __half* __restrict__ scales,
                          __half* __restrict__ zeros) {
   constexpr int RB = GS / kSearchedRows;  // row blocks per group
@@ -495,7 +495,8 @@ __global__ void __launch_bounds__(kSearchedThreads, 3)
     sj[i + 3] = v.w;
   }
   // {1/step x8, 1.5*2^23 + zero x8, step x8} of (best candidate, group, chunk)
-  const int k = *best_idx;
+  int k = *best_idx;
+  k = k < 0 ? 0 : (k >= G ? G - 1 : k);  // awq_search always writes an index in [0, G)
   const float* qc = qp + ((static_cast<int64_t>(k) * T + g) * chunks + c) * kQChunkFloats;
   const float4* q4 = reinterpret_cast<const float4*>(qc);
   float inv[8], zmz[8];  // zmz: 1.5*2^23 + the stored offset (the zero; 8 for symmetric codes)
@@ -578,13 +579,13 @@ __global__ void __launch_bounds__(kSearchedThreads, 3)
 }
 
 template <int GS, bool SYM>
-cudaError_t launch_pack_searched_t(const void* W, const float* s, const float* qp, const int32_t* best_idx,
+cudaError_t launch_pack_searched_t(const void* W, const float* s, const float* qp, const int32_t* best_idx, int G,
                                    int64_t D_in, int64_t D_out, uint8_t* qweight, void* scales, void* zeros,
                                    cudaStream_t stream) {
   const int64_t threads = (D_in / GS) * (GS / kSearchedRows) * (D_out / kQChunkCols);
   const int64_t blocks = (threads + kSearchedThreads - 1) / kSearchedThreads;
   pack_searched_kernel<GS, SYM><<<static_cast<unsigned>(blocks), kSearchedThreads, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(W), s, qp, best_idx, D_in, D_out, qweight, static_cast<__half*>(scales),
+      static_cast<const __nv_bfloat16*>(W), s, qp, best_idx, G, D_in, D_out, qweight, static_cast<__half*>(scales),
       static_cast<__half*>(zeros));
   return cudaGetLastError();
 }
@@ -606,13 +607,13 @@ cudaError_t launch_pack(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* W,
   }
 }
 
-cudaError_t launch_pack_searched(const void* W, const float* s, const float* qp, const int32_t* best_idx, int64_t D_in,
-                                 int64_t D_out, int group_size, int symmetric, uint8_t* qweight, void* scales,
-                                 void* zeros, cudaStream_t stream) {
-#define AWQ_PACK_SEARCHED(GS)                                                                                   \
-  return symmetric ? launch_pack_searched_t<GS, true>(W, s, qp, best_idx, D_in, D_out, qweight, scales, zeros,   \
-                                                      stream)                                                  \
-                   : launch_pack_searched_t<GS, false>(W, s, qp, best_idx, D_in, D_out, qweight, scales, zeros, \
+cudaError_t launch_pack_searched(const void* W, const float* s, const float* qp, const int32_t* best_idx, int G,
+                                 int64_t D_in, int64_t D_out, int group_size, int symmetric, uint8_t* qweight,
+                                 void* scales, void* zeros, cudaStream_t stream) {
+#define AWQ_PACK_SEARCHED(GS)                                                                                      \
+  return symmetric ? launch_pack_searched_t<GS, true>(W, s, qp, best_idx, G, D_in, D_out, qweight, scales, zeros,   \
+                                                      stream)                                                     \
+                   : launch_pack_searched_t<GS, false>(W, s, qp, best_idx, G, D_in, D_out, qweight, scales, zeros, \
                                                        stream)
   switch (group_size) {
     case 64:

@@ -2,12 +2,15 @@
 // "AWQ (Activation-aware Weight Quantization)", 技术原理 - 重要通道识别的统计依据;
 // aiqz.cc article "awq-activation-aware-quantization", section 1 (I_i = E|X_i|).
 //
-// HBM-bound column reduction.  A CTA owns 256 consecutive channels: each lane
-// of a warp reads one 16-byte vector (8 bf16 channels) of a row, so a warp
-// reads 512 contiguous bytes per row; the 8 warps take interleaved rows of the
-// CTA's row slice.  Per-thread sums are fp32, the 8 warps are combined in a
-// fixed order through shared memory, and the row slices are summed in fp64 in
-// slice order by the last CTA of each column chunk to finish (a per-chunk
+// HBM-bound column reduction.  A CTA owns 256 consecutive channels and one
+// slice of rows.  Its producer thread streams the slice through a 4-stage
+// ring of 32-row x 256-channel boxes (one 16 KB tensor copy each), so a CTA
+// keeps 64 KB of X in flight with one instruction per box and the loads do
+// not depend on the SM's issue rate.  Eight consumer warps take interleaved
+// rows of each box: lane l adds the 8 channels 8l .. 8l+7.  Rows past N and
+// channels past D arrive as zeros.  Per-thread sums are fp32, the 8 warps are combined in
+// a fixed order through shared memory, and the row slices are summed in fp64
+// in slice order by the last CTA of each column chunk to finish (a per-chunk
 // ticket counter), so the result does not depend on timing.
 #include <cuda_bf16.h>
 
@@ -16,13 +19,10 @@
 
 namespace awqdev {
 
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+namespace {
+
+constexpr int kBoxBytes = kStatsBoxRows * kStatsCols * 2;  // 16 KB
+constexpr int kStatsSmem = kStatsStages * kBoxBytes;
 
 // |lo| and |hi| of a packed bf16 pair, widened exactly to fp32.
 __device__ __forceinline__ void add_abs_pair(uint32_t u, float& a0, float& a1) {
@@ -37,42 +37,99 @@ __device__ __forceinline__ void add_abs_vec(const uint4& v, float (&acc)[8]) {
   add_abs_pair(v.w, acc[6], acc[7]);
 }
 
-__global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __nv_bfloat16* __restrict__ X, int64_t N,
-                                                                 int64_t D, int64_t ldx, int64_t rows_per_split,
+}  // namespace
+
+__global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_constant__ CUtensorMap tmX, int64_t N,
+                                                                 int64_t D, int64_t rows_per_split,
                                                                  float* __restrict__ partial,
                                                                  unsigned int* __restrict__ tickets,
                                                                  float* __restrict__ mean_abs, uint32_t* status) {
+  extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(16) float red[kStatsRowLanes][kStatsCols];
+  __shared__ __align__(8) uint64_t full_bar[kStatsStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStatsStages];
+  __shared__ int abort_sh;
   __shared__ bool last;
+  volatile int* abort_flag = &abort_sh;
+
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rl = threadIdx.x >> 5;
-  const int64_t col = static_cast<int64_t>(blockIdx.x) * kStatsCols + lane * 8;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kStatsCols;
+  const int width = static_cast<int>(min(static_cast<int64_t>(kStatsCols), D - c0));  // channels of this chunk
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_split;
   const int64_t r1 = min(N, r0 + rows_per_split);
+  const int nbox = static_cast<int>((r1 - r0 + kStatsBoxRows - 1) / kStatsBoxRows);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStatsStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kStatsRowLanes);
+    }
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  if (col < D) {
-    const __nv_bfloat16* base = X + col;
-    int64_t r = r0 + rl;
-    constexpr int S = kStatsRowLanes;
-    // 8 rows in flight per thread
-    for (; r + 7 * S < r1; r += 8 * S) {
-      uint4 v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = ld_stream_v4(base + (r + i * S) * ldx);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) add_abs_vec(v[i], acc);
+
+  if (warp == kStatsRowLanes) {
+    // ------------------------------------------------------------ producer
+    // rows_per_split is a multiple of the box height, so a box never reaches
+    // into the next slice; the last slice's boxes end in zero fill past N
+    if (lane == 0) {
+      prefetch_tmap(&tmX);
+      int b = 0;
+      for (; b < nbox; ++b) {
+        const int s = b % kStatsStages;
+        if (b >= kStatsStages && !mbar_wait(&empty_bar[s], ((b / kStatsStages) + 1) & 1, status, abort_flag)) break;
+        mbar_arrive_expect_tx(&full_bar[s], kBoxBytes);
+        tma_load_2d(ring + s * kBoxBytes, &tmX, &full_bar[s], static_cast<int32_t>(c0),
+                    static_cast<int32_t>(r0 + static_cast<int64_t>(b) * kStatsBoxRows));
+      }
+      // after an abort, the copies still in flight into this CTA land before
+      // it moves on (boxes b - kStatsStages .. b - 1 may not have been consumed)
+      if (b < nbox || *abort_flag)
+        for (int j = max(0, b - kStatsStages); j < b; ++j)
+          mbar_wait(&full_bar[j % kStatsStages], (j / kStatsStages) & 1, nullptr, nullptr);
     }
-    for (; r < r1; r += S) add_abs_vec(ld_stream_v4(base + r * ldx), acc);
+  } else {
+    // ------------------------------------------------------------ consumer warps
+    const bool active = lane * 8 < width;
+    for (int b = 0; b < nbox; ++b) {
+      const int s = b % kStatsStages;
+      if (!mbar_wait(&full_bar[s], (b / kStatsStages) & 1, status, abort_flag)) break;
+      const int64_t rb = r0 + static_cast<int64_t>(b) * kStatsBoxRows;
+      const int rows = static_cast<int>(min(static_cast<int64_t>(kStatsBoxRows), r1 - rb));
+      const uint8_t* st = ring + s * kBoxBytes + lane * 16;
+      if (active) {
+        if (rows == kStatsBoxRows) {
+          uint4 v[kStatsBoxRows / kStatsRowLanes];
+#pragma unroll
+          for (int i = 0; i < kStatsBoxRows / kStatsRowLanes; ++i)
+            v[i] = *reinterpret_cast<const uint4*>(st + (warp + i * kStatsRowLanes) * (kStatsCols * 2));
+#pragma unroll
+          for (int i = 0; i < kStatsBoxRows / kStatsRowLanes; ++i) add_abs_vec(v[i], acc);
+        } else {
+          for (int r = warp; r < rows; r += kStatsRowLanes)
+            add_abs_vec(*reinterpret_cast<const uint4*>(st + r * (kStatsCols * 2)), acc);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
   }
-  float4* dst = reinterpret_cast<float4*>(&red[rl][lane * 8]);
-  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+
+  if (warp < kStatsRowLanes) {
+    float4* dst = reinterpret_cast<float4*>(&red[warp][lane * 8]);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
   __syncthreads();
   const int t = threadIdx.x;
-  const int64_t j = static_cast<int64_t>(blockIdx.x) * kStatsCols + t;
-  if (t < kStatsCols && j < D) {
+  const int64_t j = c0 + t;
+  if (t < kStatsCols && t < width) {
     float sum = 0.f;
 #pragma unroll
     for (int k = 0; k < kStatsRowLanes; ++k) sum += red[k][t];
@@ -85,18 +142,19 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __nv_bfl
   __syncthreads();
   if (!last) return;
   __threadfence();
-  if (t < kStatsCols && j < D) {
+  if (t < kStatsCols && t < width) {
+    // the slices in order, 32 loads in flight per batch (one batch unless
+    // the grid has more than 32 slices)
     const int splits = static_cast<int>(gridDim.y);
     double s = 0.0;
-    int k = 0;
-    for (; k + 8 <= splits; k += 8) {
-      float v[8];  // eight loads in flight, added in slice order
+    for (int k = 0; k < splits; k += 32) {
+      float v[32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = partial[static_cast<int64_t>(k + i) * D + j];
+      for (int i = 0; i < 32; ++i) v[i] = k + i < splits ? partial[static_cast<int64_t>(k + i) * D + j] : 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s += static_cast<double>(v[i]);
+      for (int i = 0; i < 32; ++i)
+        if (k + i < splits) s += static_cast<double>(v[i]);
     }
-    for (; k < splits; ++k) s += static_cast<double>(partial[static_cast<int64_t>(k) * D + j]);
     const float m = static_cast<float>(s / static_cast<double>(N));
     if (!isfinite(m)) set_error(status, AWQ_DEV_NONFINITE);
     mean_abs[j] = m;
@@ -106,25 +164,36 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __nv_bfl
 
 void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split) {
   const int64_t chunks = (D + kStatsCols - 1) / kStatsCols;
-  int64_t want = (kStatsTargetCtas + chunks - 1) / (chunks > 0 ? chunks : 1);
-  const int64_t max_splits = (N + 63) / 64;  // at least 64 rows per slice
+  // as many row slices as keep the grid within one resident wave
+  int64_t want = kStatsTargetCtas / (chunks > 0 ? chunks : 1);
+  const int64_t max_splits = (N + 4 * kStatsBoxRows - 1) / (4 * kStatsBoxRows);  // >= 4 boxes per slice
   if (want > max_splits) want = max_splits;
   if (want < 1) want = 1;
   if (want > kStatsMaxSplits) want = kStatsMaxSplits;
   int64_t rps = (N + want - 1) / want;
-  rps = (rps + kStatsRowLanes - 1) / kStatsRowLanes * kStatsRowLanes;
-  if (rps < kStatsRowLanes) rps = kStatsRowLanes;
+  rps = (rps + kStatsBoxRows - 1) / kStatsBoxRows * kStatsBoxRows;
   *rows_per_split = rps;
   *splits = static_cast<int>((N + rps - 1) / rps);
   if (*splits < 1) *splits = 1;
 }
 
-cudaError_t launch_act_stats(const void* X, int64_t N, int64_t D, int64_t ldx, float* mean_abs, float* partial,
-                             unsigned int* tickets, int splits, int64_t rows_per_split, uint32_t* status,
-                             cudaStream_t stream) {
+cudaError_t launch_act_stats(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, int64_t N, int64_t D,
+                             int64_t ldx, float* mean_abs, float* partial, unsigned int* tickets, int splits,
+                             int64_t rows_per_split, uint32_t* status, cudaStream_t stream) {
+  CUtensorMap tm;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
+  const cuuint32_t box[2] = {kStatsCols, kStatsBoxRows};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(act_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStatsSmem);
+  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(stats_chunks(D)), static_cast<unsigned>(splits));
-  act_stats_kernel<<<grid, kStatsThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(X), N, D, ldx, rows_per_split,
-                                                       partial, tickets, mean_abs, status);
+  act_stats_kernel<<<grid, kStatsThreads, kStatsSmem, stream>>>(tm, N, D, rows_per_split, partial, tickets, mean_abs,
+                                                                status);
   return cudaGetLastError();
 }
 

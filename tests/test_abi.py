@@ -108,5 +108,15 @@ def test_calls_validate_before_cuda(L):
     assert L.awq_quantize_pack(fake, fake, 200, 256, ctypes.byref(cfg), fake, fake, fake, fake, 256, None) == 2
     assert L.awq_quantize_pack(fake, fake, 256, 256, ctypes.byref(cfg), ctypes.c_void_p(0x1001), fake, fake, fake,
                                256, None) == 3
+    # pack after a search: grid size out of range, group does not divide D_in,
+    # misaligned s_star, workspace without the parameter table; empty is a no-op
+    ps = L.awq_quantize_pack_searched
+    assert ps(fake, 256, 256, 0, ctypes.byref(cfg), fake, 1 << 40, fake, fake, fake, fake, fake, None) == 2
+    assert ps(fake, 200, 256, 21, ctypes.byref(cfg), fake, 1 << 40, fake, fake, fake, fake, fake, None) == 2
+    assert ps(fake, 256, 252, 21, ctypes.byref(cfg), fake, 1 << 40, fake, fake, fake, fake, fake, None) == 2
+    assert ps(fake, 256, 256, 21, ctypes.byref(cfg), fake, 1 << 40, fake, ctypes.c_void_p(0x1004), fake, fake, fake,
+              None) == 3
+    assert ps(fake, 256, 256, 21, ctypes.byref(cfg), fake, 4096, fake, fake, fake, fake, fake, None) == 4
+    assert ps(fake, 0, 256, 21, ctypes.byref(cfg), fake, 0, fake, fake, fake, fake, fake, None) == 0
     # self-test GEMM: K not a multiple of 64
     assert L.awq_selftest_gemm_bf16(fake, fake, 1, 128, 256, 100, fake, fake, 256, None) == 2
