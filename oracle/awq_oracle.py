@@ -239,6 +239,31 @@ def unpack_codes(qweight: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# After the path: the W4A16 inference product on the packed layer.
+# [concept] 推理时的等效实现: offline W_quantized = Quantize(diag(s*) W) with
+# s* kept as metadata; online Y = (X diag(1/s*)) Dequant(W_quantized), the
+# 1/s* scaling optionally folded into the kernel's dequantisation
+# (ASCII 架构图: "Dequant + MatMul (融合 s* 缩放)").  Dequant is the
+# quantiser's inverse, (code - zero) * scale per group (量化数学基础 step 3).
+# ---------------------------------------------------------------------------
+def w4a16_matmul(X, qweight, scales, zeros, s, group_size=128):
+    """Y = (X diag(1/s)) Dequant(qweight) in float64.
+
+    X [M, D_in] (any float type, taken exactly), qweight uint8 [D_in/2, D_out]
+    in the pack layout, scales / zeros fp16 [D_in/group_size, D_out], s fp32
+    [D_in] (None: no scaling).  Returns float64 [M, D_out].
+    """
+    codes = unpack_codes(qweight).astype(np.float64)             # [D_in, D_out]
+    D_in, D_out = codes.shape
+    g = np.arange(D_in) // group_size                            # group of each input row
+    Wq = (codes - np.asarray(zeros, dtype=np.float64)[g, :]) * np.asarray(scales, dtype=np.float64)[g, :]
+    X64 = np.asarray(X, dtype=np.float64)
+    if s is not None:
+        X64 = X64 / np.asarray(s, dtype=np.float64)[None, :]     # X diag(1/s), elementwise
+    return X64 @ Wq
+
+
+# ---------------------------------------------------------------------------
 # Diagnostic: relative activation-weighted error, [aiqz] section 5
 # epsilon = E||X (W - W_hat)||^2 / E||X W||^2.
 # ---------------------------------------------------------------------------

@@ -281,3 +281,75 @@ def check_zero_point_is_canonical(orc):
 
 
 ALL_CHECKS.append(check_zero_point_is_canonical)
+
+
+# ---------------------------------------------------------------- W4A16 product
+def check_w4a16_hand_bytes(orc):
+    """Two groups of two rows, two columns: every code, zero, scale and 1/s
+    worked by hand from (code - zero) * scale / s_j."""
+    qweight = np.array([[0x3A, 0x0F], [0x81, 0x77]], dtype=np.uint8)
+    scales = np.array([[0.5, 1.0], [0.25, 2.0]], dtype=np.float16)
+    zeros = np.array([[8, 0], [8, 5]], dtype=np.float16)
+    s = np.array([1.0, 2.0, 4.0, 0.5], dtype=F32)
+    X = np.vstack([np.eye(4), np.ones((1, 4))]).astype(F32)
+    # column 0: codes 10, 3, 1, 8 -> 1.0, -2.5, -1.75, 0 -> / s -> 1.0, -1.25, -0.4375, 0
+    # column 1: codes 15, 0, 7, 7 -> 15, 0, 4, 4      -> / s -> 15, 0, 1, 8
+    want = np.array([[1.0, 15.0], [-1.25, 0.0], [-0.4375, 1.0], [0.0, 8.0], [-0.6875, 24.0]])
+    Y = orc.w4a16_matmul(X, qweight, scales, zeros, s, group_size=2)
+    assert np.array_equal(Y, want), Y
+    # without s the dequantised weights themselves
+    Y = orc.w4a16_matmul(np.eye(4, dtype=F32), qweight, scales, zeros, None, group_size=2)
+    assert np.array_equal(Y, np.array([[1.0, 15.0], [-2.5, 0.0], [-1.75, 4.0], [0.0, 4.0]]))
+
+
+def _grid_layer(rng, D_in, D_out, g, sym):
+    """W = (q - z) * step / s with power-of-two steps and scales: weights that
+    the quantiser reproduces exactly (each group-column holds both ends of its
+    code range, so the range gives back the same step and zero)."""
+    T = D_in // g
+    e = rng.integers(-9, -3, size=(T, D_out))
+    step = np.ldexp(1.0, e)
+    if sym:
+        q = rng.integers(-7, 8, size=(T, g, D_out)).astype(np.float64)
+        q[:, 0, :] = np.where(rng.random((T, D_out)) < 0.5, 7.0, -7.0)
+        z = np.zeros((T, D_out))
+    else:
+        z = rng.integers(0, 16, size=(T, D_out)).astype(np.float64)
+        q = rng.integers(0, 16, size=(T, g, D_out)).astype(np.float64)
+        q[:, 0, :] = 0.0
+        q[:, 1, :] = 15.0
+        q = q - z[:, None, :]
+    s = np.ldexp(1.0, rng.integers(-3, 4, size=D_in))
+    Wp = (q * step[:, None, :]).reshape(D_in, D_out)
+    return (Wp / s[:, None]).astype(F32), s.astype(F32)
+
+
+def check_w4a16_grid_roundtrip(orc, seed=8):
+    """On weights the quantiser reproduces exactly, pack followed by the
+    W4A16 product is the plain product X W."""
+    rng = _rng(seed)
+    for sym in (False, True):
+        W, s = _grid_layer(rng, 64, 24, 16, sym)
+        X = rng.standard_normal((9, 64)).astype(F32)
+        qw, sc, z = orc.pack(W, s, group_size=16, symmetric=sym)
+        Y = orc.w4a16_matmul(X, qw, sc, z, s, group_size=16)
+        ref = X.astype(np.float64) @ W.astype(np.float64)
+        np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def check_w4a16_error_bound(orc, seed=9):
+    """Off the grid: |Y - X W| <= sum_j |x_j| / s_j * step_jn * (1/2 + 2^-6)."""
+    rng = _rng(seed)
+    for sym in (False, True):
+        W = (rng.standard_normal((128, 40)) * 0.02).astype(F32)
+        s = rng.uniform(0.5, 20.0, 128).astype(F32)
+        X = rng.standard_normal((6, 128)).astype(F32)
+        qw, sc, z = orc.pack(W, s, group_size=32, symmetric=sym)
+        Y = orc.w4a16_matmul(X, qw, sc, z, s, group_size=32)
+        ref = X.astype(np.float64) @ W.astype(np.float64)
+        step_rows = np.repeat(sc.astype(np.float64), 32, axis=0)           # [D_in, D_out]
+        bound = (np.abs(X.astype(np.float64)) / s.astype(np.float64)[None, :]) @ (step_rows * (0.5 + 2.0 ** -6))
+        assert np.all(np.abs(Y - ref) <= bound * (1 + 1e-9) + 1e-12)
+
+
+ALL_CHECKS += [check_w4a16_hand_bytes, check_w4a16_grid_roundtrip, check_w4a16_error_bound]

@@ -35,6 +35,12 @@ MUTANTS = [
     ("loss_abs_not_square", "return (E * E).sum(axis=0)", "return np.abs(E).sum(axis=0)"),
     ("argmax_not_argmin", "best = int(np.argmin(losses))", "best = int(np.argmax(losses))"),
     ("nibbles_swapped", "qweight = (lo | (hi << 4)).astype(np.uint8)", "qweight = (hi | (lo << 4)).astype(np.uint8)"),
+    ("w4a16_nibbles_swapped", "codes = unpack_codes(qweight).astype(np.float64)             # [D_in, D_out]",
+     "codes = unpack_codes(((qweight >> 4) | (qweight << 4)).astype(np.uint8)).astype(np.float64)"),
+    ("w4a16_drops_zero", "Wq = (codes - np.asarray(zeros, dtype=np.float64)[g, :])", "Wq = (codes - 0 * np.asarray(zeros, dtype=np.float64)[g, :])"),
+    ("w4a16_scales_not_divides", "X64 = X64 / np.asarray(s, dtype=np.float64)[None, :]", "X64 = X64 * np.asarray(s, dtype=np.float64)[None, :]"),
+    ("w4a16_group_index_mod", "g = np.arange(D_in) // group_size", "g = np.arange(D_in) % (D_in // group_size)"),
+    ("w4a16_group_of_pairs", "g = np.arange(D_in) // group_size", "g = (np.arange(D_in) // 2) // group_size"),
     ("alpha_scaled_twice", "return np.power(a.astype(np.float64), np.float64(alpha)).astype(F32)",
      "return np.power(a.astype(np.float64), np.float64(2 * alpha)).astype(F32)"),
 ]
