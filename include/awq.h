@@ -219,6 +219,32 @@ AWQ_API awq_status awq_quantize_pack_searched(const void* W, int64_t D_in, int64
                                               const int32_t* best_idx, const float* s_star, uint8_t* qweight,
                                               void* scales, void* zeros, awq_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * After the path: the W4A16 product on the packed layer.
+ *
+ * "AWQ (Activation-aware Weight Quantization)", 推理时的等效实现: the layer is
+ * stored as W_quantized = Quantize(diag(s*) W) with s* as metadata, and at
+ * inference Y = (X diag(1/s*)) Dequant(W_quantized), the 1/s* scaling folded
+ * into the kernel's dequantisation (the pipeline figure's "Dequant + MatMul
+ * (融合 s* 缩放)"); Dequant = (code - zero) * scale per group.
+ *
+ *   X        device, bf16 [M, D_in] contiguous (the layer's input activations)
+ *   qweight, scales, zeros   device, the outputs of awq_quantize_pack (or
+ *            awq_quantize_pack_searched) for this layer and cfg->group_size
+ *   s        device, fp32 [D_in]: the s* the layer was packed with, or NULL
+ *            for the plain product X Dequant(qweight)
+ *   Y        device, bf16 [M, D_out] contiguous (written)
+ *   ws       device workspace of at least 256 bytes (status word)
+ * Each weight enters the tensor cores as bf16(((code - zero) * scale) *
+ * RN(1/s_j)) and the products accumulate in fp32; Y is that sum rounded to
+ * bf16.  Shapes: D_in a multiple of 64 and of group_size, D_out a multiple of
+ * 16; all pointers 16-byte aligned (ws 256).  M = 0 is a no-op.  A timeout
+ * of the kernel's bounded waits sets AWQ_ERR_TIMEOUT in the status word.
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_w4a16_matmul(const void* X, int64_t M, int64_t D_in, int64_t D_out, const uint8_t* qweight,
+                                    const void* scales, const void* zeros, const float* s, const awq_cfg* cfg,
+                                    void* Y, void* ws, size_t ws_bytes, awq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -62,6 +62,8 @@ _SIGS = {
                           ctypes.c_int),
     "awq_quantize_pack_searched": ([_vp, _c_i64, _c_i64, _c_i32, ctypes.POINTER(awq_cfg), _vp, _c_sz, _vp, _vp,
                                     _vp, _vp, _vp, _vp], ctypes.c_int),
+    "awq_w4a16_matmul": ([_vp, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp, ctypes.POINTER(awq_cfg), _vp, _vp, _c_sz,
+                          _vp], ctypes.c_int),
     "awq_selftest_gemm_bf16": ([_vp, _vp, _c_i32, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_sz, _vp], ctypes.c_int),
     "awq_profile_enable": ([_c_i32], ctypes.c_int),
     "awq_profile_collect": ([ctypes.POINTER(awq_kernel_time), _c_i32, ctypes.POINTER(_c_i32)], ctypes.c_int),
@@ -268,6 +270,34 @@ def quantize_pack_searched(W: torch.Tensor, result: SearchResult, group_size: in
                                             _ptr(scales), _ptr(zeros), _stream_handle(stream)),
            "awq_quantize_pack_searched")
     return qweight, scales, zeros
+
+
+# ---------------------------------------------------------------------- after the path
+def w4a16_matmul(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+                 s: Optional[torch.Tensor] = None, group_size: int = 128, out: Optional[torch.Tensor] = None,
+                 ws: Optional[torch.Tensor] = None, stream=None, check: bool = True) -> torch.Tensor:
+    """Y = (X diag(1/s)) Dequant(qweight), bf16 [M, D_out]: the inference product on a packed layer."""
+    _need(X, torch.bfloat16, "X")
+    _need(qweight, torch.uint8, "qweight")
+    _need(scales, torch.float16, "scales")
+    _need(zeros, torch.float16, "zeros")
+    if s is not None:
+        _need(s, torch.float32, "s")
+    M, D_in = X.shape
+    D_out = qweight.shape[1]
+    if qweight.shape[0] * 2 != D_in:
+        raise ValueError("qweight must be [D_in/2, D_out]")
+    if out is None:
+        out = torch.empty(M, D_out, dtype=torch.bfloat16, device=X.device)
+    if ws is None:
+        ws = _alloc_ws(256, X.device)
+    cfg = make_cfg(group_size)
+    _check(lib().awq_w4a16_matmul(_ptr(X), M, D_in, D_out, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(s),
+                                  ctypes.byref(cfg), _ptr(out), _ptr(ws), ws.numel(), _stream_handle(stream)),
+           "awq_w4a16_matmul")
+    if check:
+        check_workspace(ws, "awq_w4a16_matmul (device)", stream)
+    return out
 
 
 # ---------------------------------------------------------------------- self-test

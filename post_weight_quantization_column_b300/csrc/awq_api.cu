@@ -30,6 +30,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 std::mutex g_mu;
 int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
 int g_pairs[kMaxDevices];    // resident CTA pairs of the fused search (0 = not queried)
+int g_w4a16_pairs[kMaxDevices];  // resident CTA pairs of the W4A16 product (0 = not queried)
 int g_sms[kMaxDevices];      // multiprocessor count (0 = not queried)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -75,6 +76,17 @@ awq_status get_sms(int dev, int* sms) {
     g_sms[dev] = n;
   }
   *sms = g_sms[dev];
+  return AWQ_OK;
+}
+
+awq_status get_w4a16_pairs(int dev, int* pairs) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_w4a16_pairs[dev] == 0) {
+    int n = 0;
+    if (w4a16_max_pairs(&n) != cudaSuccess || n < 1) return AWQ_ERR_CUDA;
+    g_w4a16_pairs[dev] = n;
+  }
+  *pairs = g_w4a16_pairs[dev];
   return AWQ_OK;
 }
 
@@ -405,6 +417,37 @@ awq_status awq_quantize_pack_searched(const void* W, int64_t D_in, int64_t D_out
   ProfScope prof("pack_searched", cs);
   return from_cuda(launch_pack_searched(W, s_star, qp, best_idx, G, D_in, D_out, cfg->group_size, cfg->symmetric,
                                         qweight, scales, zeros, cs));
+}
+
+// ------------------------------------------------------------------ W4A16 product
+awq_status awq_w4a16_matmul(const void* X, int64_t M, int64_t D_in, int64_t D_out, const uint8_t* qweight,
+                            const void* scales, const void* zeros, const float* s, const awq_cfg* cfg, void* Y,
+                            void* ws, size_t ws_bytes, awq_stream_t stream) {
+  awq_status st = validate_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (M < 0 || D_in < 0 || D_out < 0) return AWQ_ERR_SHAPE;
+  if (D_in % 64 != 0 || D_in % cfg->group_size != 0 || D_out % 16 != 0) return AWQ_ERR_SHAPE;
+  if (M > INT32_MAX || D_in > INT32_MAX || D_out > INT32_MAX) return AWQ_ERR_SHAPE;
+  if (M == 0 || D_in == 0 || D_out == 0) return AWQ_OK;
+  if (!X || !qweight || !scales || !zeros || !Y || !ws) return AWQ_ERR_INVALID_ARG;
+  if (!aligned(X, 16) || !aligned(qweight, 16) || !aligned(scales, 16) || !aligned(zeros, 16) ||
+      (s && !aligned(s, 16)) || !aligned(Y, 16) || !aligned(ws, 256))
+    return AWQ_ERR_ALIGNMENT;
+  if (ws_bytes < kHeaderBytes) return AWQ_ERR_WORKSPACE;
+  int dev = 0;
+  st = check_device(&dev);
+  if (st != AWQ_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  st = get_encode(&encode);
+  if (st != AWQ_OK) return st;
+  int pairs = 0;
+  st = get_w4a16_pairs(dev, &pairs);
+  if (st != AWQ_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return AWQ_ERR_CUDA;
+  ProfScope prof("w4a16", cs);
+  return from_cuda(launch_w4a16(encode, X, M, D_in, D_out, qweight, scales, zeros, s, cfg->group_size, Y,
+                                status_word(ws), pairs, cs));
 }
 
 // ------------------------------------------------------------------ self-test GEMM

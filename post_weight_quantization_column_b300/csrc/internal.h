@@ -79,6 +79,11 @@ cudaError_t launch_gemm_store(PFN_cuTensorMapEncodeTiled_v12000 encode, const vo
 int search_fused_m_tiles(int64_t N);
 // CTA pairs that fit on the device at once (occupancy query).
 cudaError_t search_fused_max_pairs(int* pairs);
+// W4A16 product Y = (X diag(1/s)) Dequant(qweight) on CTA pairs (s may be null).
+cudaError_t w4a16_max_pairs(int* pairs);
+cudaError_t launch_w4a16(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, int64_t M, int64_t D_in,
+                         int64_t D_out, const uint8_t* qweight, const void* scales, const void* zeros, const float* s,
+                         int group_size, void* Y, uint32_t* status, int max_pairs, cudaStream_t stream);
 cudaError_t launch_search_fused(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, const void* W,
                                 const float* s_tab, const float* r_tab, const float* qp, int64_t N, int64_t D_in,
                                 int64_t D_out, int G, int group_size, int symmetric, float* partial,

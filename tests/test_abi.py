@@ -118,5 +118,14 @@ def test_calls_validate_before_cuda(L):
               None) == 3
     assert ps(fake, 256, 256, 21, ctypes.byref(cfg), fake, 4096, fake, fake, fake, fake, fake, None) == 4
     assert ps(fake, 0, 256, 21, ctypes.byref(cfg), fake, 0, fake, fake, fake, fake, fake, None) == 0
+    # W4A16 product: D_in not a multiple of 64, D_out not a multiple of 16,
+    # misaligned Y, workspace too small; no rows is a no-op
+    mm = L.awq_w4a16_matmul
+    assert mm(fake, 8, 96, 256, fake, fake, fake, None, ctypes.byref(cfg), fake, fake, 256, None) == 2
+    assert mm(fake, 8, 256, 264, fake, fake, fake, None, ctypes.byref(cfg), fake, fake, 256, None) == 2
+    assert mm(fake, 8, 256, 256, fake, fake, fake, None, ctypes.byref(cfg), ctypes.c_void_p(0x1008), fake, 256,
+              None) == 3
+    assert mm(fake, 8, 256, 256, fake, fake, fake, None, ctypes.byref(cfg), fake, fake, 16, None) == 4
+    assert mm(fake, 0, 256, 256, fake, fake, fake, None, ctypes.byref(cfg), fake, fake, 256, None) == 0
     # self-test GEMM: K not a multiple of 64
     assert L.awq_selftest_gemm_bf16(fake, fake, 1, 128, 256, 100, fake, fake, 256, None) == 2
