@@ -447,6 +447,30 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
     e2e_ms = max_over_ranks(e2e_ms, world)
+
+    # ---- after the path: the W4A16 product of the step's packed layer on its
+    # own activations, Y = (X diag(1/s*)) Dequant(qweight); separate from the step
+    w4 = None
+    if Do % 16 == 0 and Di % 64 == 0:
+        Y = torch.empty(N, Do, dtype=torch.bfloat16, device=dev)
+        ws_y = torch.empty(256, dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            awq.w4a16_matmul(Xd, *pk, res.s_star, g, out=Y, ws=ws_y, check=False)
+        awq.check_workspace(ws_y, "w4a16")
+        y_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+        for i in range(10):
+            flush_l2()
+            y_ev[i][0].record()
+            awq.w4a16_matmul(Xd, *pk, res.s_star, g, out=Y, ws=ws_y, check=False)
+            y_ev[i][1].record()
+        torch.cuda.synchronize()
+        awq.check_workspace(ws_y, "w4a16")
+        y_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in y_ev)[5], world)
+        y_tf = 2.0 * N * Di * Do / (y_ms * 1e-3) / 1e12
+        w4 = {"workload": f"Y = (X diag(1/s*)) Dequant(qweight), M={N} D_in={Di} D_out={Do}, bf16 out",
+              "ms": y_ms, "tflops": y_tf, "bound": "tensor", "peak": peaks["bf16_tflops"],
+              "frac": y_tf / peaks["bf16_tflops"], "timing": "median of 10 launches, L2 flushed before each"}
+        del Y
     for ws, nm in ((ws_s, "act_stats"), (ws_q, "search")):
         awq.check_workspace(ws, nm)
 
@@ -468,6 +492,7 @@ def run_ours(args, world, rank, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "clocks": clocks,
+        "w4a16": w4,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         Xf, Wf = synth.bf16_to_f32(X), synth.bf16_to_f32(W)

@@ -74,6 +74,38 @@ def act_stats(X: np.ndarray) -> np.ndarray:
     return (total / N).astype(F32)
 
 
+def act_stats_max(X: np.ndarray) -> np.ndarray:
+    """The alternative statistic a_j = max_r |x_rj| ([concept] 二、缩放因子的搜索:
+    s_j = (max |X_j|)^alpha; 重要通道识别的统计依据: "或 max").  Exact."""
+    X = np.asarray(X)
+    if X.shape[0] == 0:
+        raise ValueError("act_stats_max needs at least one calibration row")
+    X64 = X.astype(np.float64)
+    if not np.all(np.isfinite(X64)):
+        raise OracleNonFiniteError("X holds non-finite values")
+    return np.abs(X64).max(axis=0).astype(F32)
+
+
+def act_stats_stream(batches) -> np.ndarray:
+    """The mean |x| accumulated batch by batch ([adr] Decision, Layer 2:
+    AWQQuantizer.add_batch accumulates the per-channel mean-abs activation):
+    each batch's column sums of |x| in float64 are added to a running float64
+    total in batch order, and the total is divided once by the number of rows
+    seen."""
+    total = None
+    rows = 0
+    for X in batches:
+        X64 = np.asarray(X).astype(np.float64)
+        if not np.all(np.isfinite(X64)):
+            raise OracleNonFiniteError("X holds non-finite values")
+        part = np.abs(X64).sum(axis=0)
+        total = part if total is None else total + part
+        rows += X64.shape[0]
+    if rows == 0:
+        raise ValueError("act_stats_stream needs at least one calibration row")
+    return (total / rows).astype(F32)
+
+
 # ---------------------------------------------------------------------------
 # Step 2a: candidate scale family
 # [concept] 缩放因子优化的完整流程 step 3: s_j(alpha) = activation_scale[j]^alpha,

@@ -353,3 +353,35 @@ def check_w4a16_error_bound(orc, seed=9):
 
 
 ALL_CHECKS += [check_w4a16_hand_bytes, check_w4a16_grid_roundtrip, check_w4a16_error_bound]
+
+
+# ---------------------------------------------------------------- streaming statistic and max variant
+def check_act_stats_max_closed_forms(orc):
+    X = np.array([[1.0, -2.0, 0.0], [-3.5, 0.5, 0.0], [2.0, -0.25, 0.0]], dtype=F32)
+    assert np.array_equal(orc.act_stats_max(X), np.array([3.5, 2.0, 0.0], dtype=F32))
+    # one row: |x| itself; max >= mean everywhere
+    rng = _rng(10)
+    X = rng.standard_normal((9, 7)).astype(F32)
+    assert np.array_equal(orc.act_stats_max(X[:1]), np.abs(X[0]))
+    assert np.all(orc.act_stats_max(X) >= orc.act_stats(X))
+
+
+def check_act_stats_stream_matches_single_shot(orc):
+    """On dyadic inputs every float64 sum is exact, so the batch-by-batch mean
+    equals the one-shot mean bit for bit whatever the split; and a batch of
+    constant |x| = c gives c."""
+    rng = _rng(11)
+    X = (rng.integers(-64, 65, size=(37, 6)) / 8.0).astype(F32)
+    one = orc.act_stats(X)
+    for cuts in ([37], [5, 32], [1, 1, 35], [12, 12, 13]):
+        parts = np.split(X, np.cumsum(cuts)[:-1])
+        assert np.array_equal(orc.act_stats_stream(parts), one)
+    c = np.full((4, 3), -0.375, dtype=F32)
+    assert np.array_equal(orc.act_stats_stream([c, c[:1]]), np.full(3, 0.375, dtype=F32))
+    # the running total is divided by the rows of all batches, not averaged per batch
+    a = np.ones((1, 2), dtype=F32)
+    b = np.zeros((3, 2), dtype=F32)
+    assert np.array_equal(orc.act_stats_stream([a, b]), np.full(2, 0.25, dtype=F32))
+
+
+ALL_CHECKS += [check_act_stats_max_closed_forms, check_act_stats_stream_matches_single_shot]

@@ -41,6 +41,9 @@ MUTANTS = [
     ("w4a16_scales_not_divides", "X64 = X64 / np.asarray(s, dtype=np.float64)[None, :]", "X64 = X64 * np.asarray(s, dtype=np.float64)[None, :]"),
     ("w4a16_group_index_mod", "g = np.arange(D_in) // group_size", "g = np.arange(D_in) % (D_in // group_size)"),
     ("w4a16_group_of_pairs", "g = np.arange(D_in) // group_size", "g = (np.arange(D_in) // 2) // group_size"),
+    ("max_stat_no_abs", "return np.abs(X64).max(axis=0).astype(F32)", "return X64.max(axis=0).astype(F32)"),
+    ("stream_mean_of_batch_means", "total = part if total is None else total + part\n        rows += X64.shape[0]",
+     "part = part / X64.shape[0]\n        total = part if total is None else total + part\n        rows += 1"),
     ("alpha_scaled_twice", "return np.power(a.astype(np.float64), np.float64(alpha)).astype(F32)",
      "return np.power(a.astype(np.float64), np.float64(2 * alpha)).astype(F32)"),
 ]
