@@ -110,6 +110,31 @@ AWQ_API awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t
                          float* mean_abs, void* ws, size_t ws_bytes, awq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The statistic over a stream of calibration batches, and its max variant.
+ *
+ * "009. AWQ Integration", Decision (Layer 2): the quantizer's add_batch
+ * accumulates the per-channel mean |x| batch by batch; "AWQ (Activation-aware
+ * Weight Quantization)", 二、缩放因子的搜索 / 重要通道识别的统计依据: the
+ * statistic may also be max |X_j| ("或 max"), s_j = (max |X_j|)^alpha.
+ *
+ * awq_act_stats_accumulate adds one batch:
+ *   X, N, D_in, ldx   the batch, as for awq_act_stats (N >= 1 rows)
+ *   sum_abs  device, fp64 [D_in], read and written: sum_abs[j] += sum_r |X[r, j]|
+ *            (the batch's sum formed in the same fixed order as awq_act_stats)
+ *   max_abs  device, fp32 [D_in] or NULL: max_abs[j] = max(max_abs[j], max_r |X[r, j]|)
+ *   ws       as for awq_act_stats
+ * The caller zeroes sum_abs and max_abs before the first batch and orders the
+ * batches on one stream.  awq_act_stats_finalize writes mean_abs[j] =
+ * fp32(sum_abs[j] / rows) for rows = the total number of rows accumulated.
+ * Either vector (mean or max) can then be passed to awq_search as its
+ * statistic.  A non-finite batch sets AWQ_ERR_NONFINITE in ws.
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_act_stats_accumulate(const void* X, int64_t N, int64_t D_in, int64_t ldx, double* sum_abs,
+                                            float* max_abs, void* ws, size_t ws_bytes, awq_stream_t stream);
+AWQ_API awq_status awq_act_stats_finalize(const double* sum_abs, int64_t rows, int64_t D_in, float* mean_abs,
+                                          awq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * The same statistic for callers that cannot allocate device memory.
  * (No counterpart on the pages: this is a library convenience.)
  *

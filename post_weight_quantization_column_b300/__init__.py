@@ -53,6 +53,8 @@ _SIGS = {
     "awq_workspace_status": ([_vp, _vp], ctypes.c_int),
     "awq_act_stats_workspace_size": ([_c_i64, _c_i64, ctypes.POINTER(_c_sz)], ctypes.c_int),
     "awq_act_stats": ([_vp, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_sz, _vp], ctypes.c_int),
+    "awq_act_stats_accumulate": ([_vp, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _c_sz, _vp], ctypes.c_int),
+    "awq_act_stats_finalize": ([_vp, _c_i64, _c_i64, _vp, _vp], ctypes.c_int),
     "awq_search_workspace_size": ([_c_i64, _c_i64, _c_i64, _c_i32, ctypes.POINTER(awq_cfg),
                                    ctypes.POINTER(_c_sz)], ctypes.c_int),
     "awq_search": ([_vp, _vp, _c_i64, _c_i64, _c_i64, _vp, ctypes.POINTER(ctypes.c_double), _c_i32,
@@ -156,6 +158,48 @@ def act_stats(X: torch.Tensor, out: Optional[torch.Tensor] = None, ws: Optional[
     if check:
         check_workspace(ws, "awq_act_stats (device)", stream)
     return out
+
+
+class StatsAccumulator:
+    """The statistic over a stream of calibration batches (the ADR's add_batch):
+    float64 running column sums of |x| and, optionally, the running max |x|."""
+
+    def __init__(self, D_in: int, device, track_max: bool = False):
+        self.D_in = D_in
+        self.rows = 0
+        self.sum_abs = torch.zeros(D_in, dtype=torch.float64, device=device)
+        self.max_abs = torch.zeros(D_in, dtype=torch.float32, device=device) if track_max else None
+        self._ws = None
+
+    def add_batch(self, X: torch.Tensor, stream=None, check: bool = True):
+        _need(X, torch.bfloat16, "X")
+        N, D = X.shape
+        if D != self.D_in:
+            raise ValueError("batch has the wrong number of channels")
+        need = act_stats_workspace_size(N, D)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = _alloc_ws(need, X.device)
+        _check(lib().awq_act_stats_accumulate(_ptr(X), N, D, D, _ptr(self.sum_abs), _ptr(self.max_abs),
+                                              _ptr(self._ws), self._ws.numel(), _stream_handle(stream)),
+               "awq_act_stats_accumulate")
+        if check:
+            check_workspace(self._ws, "awq_act_stats_accumulate (device)", stream)
+        self.rows += N
+        return self
+
+    def mean(self, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty(self.D_in, dtype=torch.float32, device=self.sum_abs.device)
+        _check(lib().awq_act_stats_finalize(_ptr(self.sum_abs), self.rows, self.D_in, _ptr(out),
+                                            _stream_handle(stream)), "awq_act_stats_finalize")
+        return out
+
+
+def act_stats_max(X: torch.Tensor, stream=None) -> torch.Tensor:
+    """max_r |X[r, j]| for X bf16 [N, D_in] on the GPU -> fp32 [D_in] (exact)."""
+    acc = StatsAccumulator(X.shape[1], X.device, track_max=True)
+    acc.add_batch(X, stream=stream)
+    return acc.max_abs
 
 
 # ---------------------------------------------------------------------- steps 2-3

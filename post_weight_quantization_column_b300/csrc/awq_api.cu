@@ -159,13 +159,17 @@ awq_status validate_cfg(const awq_cfg* cfg) {
 uint32_t* status_word(void* ws) { return static_cast<uint32_t*>(ws); }
 
 // ---------------------------------------------------------------- layouts
-// act_stats workspace: header (status word) | tickets [stats_chunks] | partials [splits][D_in]
+// act_stats workspace: header (status word) | tickets [stats_chunks] |
+// partial sums [splits][D_in] | partial maxima [splits][D_in]
 size_t stats_ticket_bytes(int64_t D_in) { return align_up(static_cast<size_t>(stats_chunks(D_in)) * 4, 256); }
-size_t stats_ws_bytes(int64_t N, int64_t D_in) {
+size_t stats_partial_bytes(int64_t N, int64_t D_in) {
   int splits = 1;
   int64_t rps = 0;
   stats_plan(N, D_in, &splits, &rps);
-  return kHeaderBytes + stats_ticket_bytes(D_in) + align_up(static_cast<size_t>(splits) * static_cast<size_t>(D_in) * 4, 256);
+  return align_up(static_cast<size_t>(splits) * static_cast<size_t>(D_in) * 4, 256);
+}
+size_t stats_ws_bytes(int64_t N, int64_t D_in) {
+  return kHeaderBytes + stats_ticket_bytes(D_in) + 2 * stats_partial_bytes(N, D_in);
 }
 
 struct SearchLayout {
@@ -256,13 +260,19 @@ awq_status awq_act_stats_workspace_size(int64_t N, int64_t D_in, size_t* bytes) 
   return AWQ_OK;
 }
 
-awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t ldx, float* mean_abs, void* ws,
-                         size_t ws_bytes, awq_stream_t stream) {
+namespace {
+// One pass of the statistic kernel over X: the mean into mean_abs, or (when
+// sum_abs is given) the float64 column sums added to sum_abs; max_abs, when
+// given, takes the running maximum of |x|.
+awq_status run_act_stats(const void* X, int64_t N, int64_t D_in, int64_t ldx, float* mean_abs, double* sum_abs,
+                         float* max_abs, void* ws, size_t ws_bytes, awq_stream_t stream, const char* name) {
   if (N < 1 || D_in < 0) return AWQ_ERR_SHAPE;
   if (D_in == 0) return AWQ_OK;
-  if (!X || !mean_abs || !ws) return AWQ_ERR_INVALID_ARG;
+  if (!X || (!mean_abs && !sum_abs) || !ws) return AWQ_ERR_INVALID_ARG;
   if (ldx < D_in || D_in % 8 != 0 || ldx % 8 != 0 || N > INT32_MAX || D_in > INT32_MAX) return AWQ_ERR_SHAPE;
-  if (!aligned(X, 16) || !aligned(mean_abs, 4) || !aligned(ws, 256)) return AWQ_ERR_ALIGNMENT;
+  if (!aligned(X, 16) || (mean_abs && !aligned(mean_abs, 4)) || (sum_abs && !aligned(sum_abs, 8)) ||
+      (max_abs && !aligned(max_abs, 4)) || !aligned(ws, 256))
+    return AWQ_ERR_ALIGNMENT;
   if (ws_bytes < stats_ws_bytes(N, D_in)) return AWQ_ERR_WORKSPACE;
   awq_status st = check_device(nullptr);
   if (st != AWQ_OK) return st;
@@ -276,11 +286,37 @@ awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t ldx, fl
   // status word and the ticket counters start at zero
   const size_t tb = stats_ticket_bytes(D_in);
   if (cudaMemsetAsync(ws, 0, kHeaderBytes + tb, s) != cudaSuccess) return AWQ_ERR_CUDA;
-  unsigned int* tickets = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
-  float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kHeaderBytes + tb);
-  ProfScope prof("act_stats", s);
-  return from_cuda(
-      launch_act_stats(encode, X, N, D_in, ldx, mean_abs, partial, tickets, splits, rps, status_word(ws), s));
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  unsigned int* tickets = reinterpret_cast<unsigned int*>(base + kHeaderBytes);
+  float* partial = reinterpret_cast<float*>(base + kHeaderBytes + tb);
+  float* partial_max = reinterpret_cast<float*>(base + kHeaderBytes + tb + stats_partial_bytes(N, D_in));
+  ProfScope prof(name, s);
+  return from_cuda(launch_act_stats(encode, X, N, D_in, ldx, mean_abs, sum_abs, max_abs, partial, partial_max,
+                                    tickets, splits, rps, status_word(ws), s));
+}
+}  // namespace
+
+awq_status awq_act_stats(const void* X, int64_t N, int64_t D_in, int64_t ldx, float* mean_abs, void* ws,
+                         size_t ws_bytes, awq_stream_t stream) {
+  if (N >= 1 && D_in > 0 && !mean_abs) return AWQ_ERR_INVALID_ARG;
+  return run_act_stats(X, N, D_in, ldx, mean_abs, nullptr, nullptr, ws, ws_bytes, stream, "act_stats");
+}
+
+awq_status awq_act_stats_accumulate(const void* X, int64_t N, int64_t D_in, int64_t ldx, double* sum_abs,
+                                    float* max_abs, void* ws, size_t ws_bytes, awq_stream_t stream) {
+  if (N >= 1 && D_in > 0 && !sum_abs) return AWQ_ERR_INVALID_ARG;
+  return run_act_stats(X, N, D_in, ldx, nullptr, sum_abs, max_abs, ws, ws_bytes, stream, "act_stats_accumulate");
+}
+
+awq_status awq_act_stats_finalize(const double* sum_abs, int64_t rows, int64_t D_in, float* mean_abs,
+                                  awq_stream_t stream) {
+  if (rows < 1 || D_in < 0) return AWQ_ERR_SHAPE;
+  if (D_in == 0) return AWQ_OK;
+  if (!sum_abs || !mean_abs) return AWQ_ERR_INVALID_ARG;
+  if (!aligned(sum_abs, 8) || !aligned(mean_abs, 4)) return AWQ_ERR_ALIGNMENT;
+  awq_status st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_stats_finalize(sum_abs, rows, D_in, mean_abs, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // ------------------------------------------------------------------ search

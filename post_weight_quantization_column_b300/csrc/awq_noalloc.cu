@@ -80,7 +80,8 @@ extern "C" awq_status awq_act_stats_noalloc(const void* X, int64_t N, int64_t D_
   const int64_t chunks = awqdev::stats_chunks(D_in);
   if (cudaMemsetAsync(tickets, 0, static_cast<size_t>(chunks) * sizeof(unsigned int), s) != cudaSuccess)
     return AWQ_ERR_CUDA;
-  const cudaError_t e = awqdev::launch_act_stats(encode, X, N, D_in, ldx, mean_abs, scratch + kNoAllocTicketWords,
-                                                 tickets, splits, rps, nullptr, s);
+  const cudaError_t e = awqdev::launch_act_stats(encode, X, N, D_in, ldx, mean_abs, nullptr, nullptr,
+                                                 scratch + kNoAllocTicketWords, nullptr, tickets, splits, rps,
+                                                 nullptr, s);
   return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
 }

@@ -37,13 +37,42 @@ __device__ __forceinline__ void add_abs_vec(const uint4& v, float (&acc)[8]) {
   add_abs_pair(v.w, acc[6], acc[7]);
 }
 
+// The same, also keeping the running max of |x| per channel (exact).
+__device__ __forceinline__ void add_max_abs_pair(uint32_t u, float& a0, float& a1, float& m0, float& m1) {
+  const float x0 = __uint_as_float((u << 16) & 0x7FFFFFFFu);
+  const float x1 = __uint_as_float(u & 0x7FFF0000u);
+  a0 += x0;
+  a1 += x1;
+  m0 = fmaxf(m0, x0);
+  m1 = fmaxf(m1, x1);
+}
+
+template <bool kMax>
+__device__ __forceinline__ void add_vec(const uint4& v, float (&acc)[8], float (&mx)[8]) {
+  if (kMax) {
+    add_max_abs_pair(v.x, acc[0], acc[1], mx[0], mx[1]);
+    add_max_abs_pair(v.y, acc[2], acc[3], mx[2], mx[3]);
+    add_max_abs_pair(v.z, acc[4], acc[5], mx[4], mx[5]);
+    add_max_abs_pair(v.w, acc[6], acc[7], mx[6], mx[7]);
+  } else {
+    add_abs_vec(v, acc);
+  }
+}
+
 }  // namespace
 
+// mean_abs: written with the mean when sum_abs is null.  sum_abs: when given,
+// the slice total of each channel (float64) is added to it instead.  max_abs:
+// when kMax, max(max_abs, the batch's max |x|) is stored back.
+template <bool kMax>
 __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_constant__ CUtensorMap tmX, int64_t N,
                                                                  int64_t D, int64_t rows_per_split,
                                                                  float* __restrict__ partial,
+                                                                 float* __restrict__ partial_max,
                                                                  unsigned int* __restrict__ tickets,
-                                                                 float* __restrict__ mean_abs, uint32_t* status) {
+                                                                 float* __restrict__ mean_abs,
+                                                                 double* __restrict__ sum_abs,
+                                                                 float* __restrict__ max_abs, uint32_t* status) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(16) float red[kStatsRowLanes][kStatsCols];
   __shared__ __align__(8) uint64_t full_bar[kStatsStages];
@@ -70,9 +99,9 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_c
   }
   __syncthreads();
 
-  float acc[8];
+  float acc[8], mx[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 8; ++i) acc[i] = mx[i] = 0.f;
 
   if (warp == kStatsRowLanes) {
     // ------------------------------------------------------------ producer
@@ -110,10 +139,10 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_c
           for (int i = 0; i < kStatsBoxRows / kStatsRowLanes; ++i)
             v[i] = *reinterpret_cast<const uint4*>(st + (warp + i * kStatsRowLanes) * (kStatsCols * 2));
 #pragma unroll
-          for (int i = 0; i < kStatsBoxRows / kStatsRowLanes; ++i) add_abs_vec(v[i], acc);
+          for (int i = 0; i < kStatsBoxRows / kStatsRowLanes; ++i) add_vec<kMax>(v[i], acc, mx);
         } else {
           for (int r = warp; r < rows; r += kStatsRowLanes)
-            add_abs_vec(*reinterpret_cast<const uint4*>(st + r * (kStatsCols * 2)), acc);
+            add_vec<kMax>(*reinterpret_cast<const uint4*>(st + r * (kStatsCols * 2)), acc, mx);
         }
       }
       __syncwarp();
@@ -135,6 +164,21 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_c
     for (int k = 0; k < kStatsRowLanes; ++k) sum += red[k][t];
     partial[static_cast<int64_t>(blockIdx.y) * D + j] = sum;
   }
+  if (kMax) {
+    __syncthreads();
+    if (warp < kStatsRowLanes) {
+      float4* dst = reinterpret_cast<float4*>(&red[warp][lane * 8]);
+      dst[0] = make_float4(mx[0], mx[1], mx[2], mx[3]);
+      dst[1] = make_float4(mx[4], mx[5], mx[6], mx[7]);
+    }
+    __syncthreads();
+    if (t < kStatsCols && t < width) {
+      float m = 0.f;
+#pragma unroll
+      for (int k = 0; k < kStatsRowLanes; ++k) m = fmaxf(m, red[k][t]);
+      partial_max[static_cast<int64_t>(blockIdx.y) * D + j] = m;
+    }
+  }
   // the last row slice of this column chunk to finish sums the slices
   __threadfence();
   __syncthreads();
@@ -155,11 +199,26 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_c
       for (int i = 0; i < 32; ++i)
         if (k + i < splits) s += static_cast<double>(v[i]);
     }
-    const float m = static_cast<float>(s / static_cast<double>(N));
-    if (!isfinite(m)) set_error(status, AWQ_DEV_NONFINITE);
-    mean_abs[j] = m;
+    if (!isfinite(s)) set_error(status, AWQ_DEV_NONFINITE);
+    if (sum_abs) {
+      sum_abs[j] += s;  // this CTA alone owns channel j now
+    } else {
+      mean_abs[j] = static_cast<float>(s / static_cast<double>(N));
+    }
+    if (kMax) {
+      float m = max_abs[j];
+      for (int k = 0; k < splits; ++k) m = fmaxf(m, partial_max[static_cast<int64_t>(k) * D + j]);
+      max_abs[j] = m;
+    }
   }
   if (t == 0) tickets[blockIdx.x] = 0u;  // ready for the next call
+}
+
+// mean = fp32(total / rows) after a stream of accumulated batches.
+__global__ void stats_finalize_kernel(const double* __restrict__ sum_abs, int64_t rows, int64_t D,
+                                      float* __restrict__ mean_abs) {
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (j < D) mean_abs[j] = static_cast<float>(sum_abs[j] / static_cast<double>(rows));
 }
 
 void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split) {
@@ -178,8 +237,9 @@ void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split) {
 }
 
 cudaError_t launch_act_stats(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, int64_t N, int64_t D,
-                             int64_t ldx, float* mean_abs, float* partial, unsigned int* tickets, int splits,
-                             int64_t rows_per_split, uint32_t* status, cudaStream_t stream) {
+                             int64_t ldx, float* mean_abs, double* sum_abs, float* max_abs, float* partial,
+                             float* partial_max, unsigned int* tickets, int splits, int64_t rows_per_split,
+                             uint32_t* status, cudaStream_t stream) {
   CUtensorMap tm;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
@@ -189,11 +249,26 @@ cudaError_t launch_act_stats(PFN_cuTensorMapEncodeTiled_v12000 encode, const voi
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(act_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStatsSmem);
-  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(stats_chunks(D)), static_cast<unsigned>(splits));
-  act_stats_kernel<<<grid, kStatsThreads, kStatsSmem, stream>>>(tm, N, D, rows_per_split, partial, tickets, mean_abs,
-                                                                status);
+  if (max_abs) {
+    cudaError_t e = cudaFuncSetAttribute(act_stats_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kStatsSmem);
+    if (e != cudaSuccess) return e;
+    act_stats_kernel<true><<<grid, kStatsThreads, kStatsSmem, stream>>>(
+        tm, N, D, rows_per_split, partial, partial_max, tickets, mean_abs, sum_abs, max_abs, status);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(act_stats_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kStatsSmem);
+    if (e != cudaSuccess) return e;
+    act_stats_kernel<false><<<grid, kStatsThreads, kStatsSmem, stream>>>(
+        tm, N, D, rows_per_split, partial, partial_max, tickets, mean_abs, sum_abs, max_abs, status);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stats_finalize(const double* sum_abs, int64_t rows, int64_t D, float* mean_abs,
+                                  cudaStream_t stream) {
+  stats_finalize_kernel<<<static_cast<unsigned>((D + 255) / 256), 256, 0, stream>>>(sum_abs, rows, D, mean_abs);
   return cudaGetLastError();
 }
 

@@ -118,6 +118,10 @@ def test_calls_validate_before_cuda(L):
               None) == 3
     assert ps(fake, 256, 256, 21, ctypes.byref(cfg), fake, 4096, fake, fake, fake, fake, fake, None) == 4
     assert ps(fake, 0, 256, 21, ctypes.byref(cfg), fake, 0, fake, fake, fake, fake, fake, None) == 0
+    # streaming statistic: no running sum; finalize over no rows
+    assert L.awq_act_stats_accumulate(fake, 8, 256, 256, None, None, fake, 1 << 20, None) == 1
+    assert L.awq_act_stats_accumulate(fake, 8, 256, 256, ctypes.c_void_p(0x1004), None, fake, 1 << 20, None) == 3
+    assert L.awq_act_stats_finalize(fake, 0, 256, fake, None) == 2
     # W4A16 product: D_in not a multiple of 64, D_out not a multiple of 16,
     # misaligned Y, workspace too small; no rows is a no-op
     mm = L.awq_w4a16_matmul
