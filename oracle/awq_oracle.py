@@ -244,6 +244,80 @@ def search(X, W, mean_abs, grid=None, group_size=128, symmetric=False, bits=4,
 
 
 # ---------------------------------------------------------------------------
+# The ADR's second search: per-group coordinate greedy over power-of-two
+# channel scales.  [adr] 关键设计 1: groups are independent along the input
+# dimension; within a group, each input channel in turn tries every grid
+# candidate (20 powers of two centred on 1), the whole group's
+# activation-weighted reconstruction error is evaluated with the pack's own
+# quantiser, and the best candidate is kept; 3 passes let a channel react to
+# a group maximum that a later channel enlarged.  [adr] 关键设计 2-3: the
+# error is measured in the original space (w'hat / s - w), with the exact
+# quantiser of the pack.
+# Readings (the ADR gives no formula): candidates 2^k, k = -10 .. 9; initial
+# s = 1; weight of channel j = its mean |x| (a_j, not squared); a candidate
+# replaces the current value only when strictly better, and among equally
+# good candidates the first in k order wins; channels in index order.
+# ---------------------------------------------------------------------------
+def greedy_candidates(count: int = 20, k_min: int = -10) -> np.ndarray:
+    """The power-of-two grid 2^k, k = k_min .. k_min + count - 1 (float32, exact)."""
+    return np.array([2.0 ** k for k in range(k_min, k_min + count)], dtype=F32)
+
+
+def group_error(Wg: np.ndarray, s: np.ndarray, a: np.ndarray, symmetric: bool, bits: int = 4) -> float:
+    """sum_j a_j sum_n (w'hat_jn / s_j - w_jn)^2 for one group Wg [g, D_out] (float64 sum)."""
+    Wg = np.asarray(Wg, dtype=F32)
+    s = np.asarray(s, dtype=F32)
+    g = Wg.shape[0]
+    codes, step, zero = quantize_groups(Wg * s[:, None], g, symmetric, bits)
+    What = dequantize(codes, step, zero, g)
+    D = What.astype(np.float64) / s.astype(np.float64)[:, None] - Wg.astype(np.float64)
+    return float((np.asarray(a, dtype=np.float64)[:, None] * D * D).sum())
+
+
+def greedy_search(W, mean_abs, group_size=128, symmetric=False, passes=3, candidates=None, follow=None):
+    """Per-group coordinate greedy of [adr] 关键设计 1.
+
+    Returns (s float32 [D_in], trace int [passes, D_in] of chosen candidate
+    indices, errors float64 [passes, D_in, len(candidates)] of every
+    evaluated candidate).  `follow`, if given ([passes, D_in] candidate
+    indices), replaces each decision by the given one (used to replay another
+    implementation's choices and judge each against these errors).
+    """
+    W = np.asarray(W, dtype=F32)
+    a = np.asarray(mean_abs, dtype=np.float64)
+    if candidates is None:
+        candidates = greedy_candidates()
+    cand = np.asarray(candidates, dtype=F32)
+    D_in = W.shape[0]
+    s = np.ones(D_in, dtype=F32)
+    one = int(np.flatnonzero(cand == F32(1.0))[0])
+    cur = np.full(D_in, one, dtype=np.int64)
+    trace = np.zeros((passes, D_in), dtype=np.int64)
+    errors = np.zeros((passes, D_in, len(cand)), dtype=np.float64)
+    for t in range(D_in // group_size):
+        rows = slice(t * group_size, (t + 1) * group_size)
+        Wg, ag = W[rows], a[rows]
+        for p in range(passes):
+            for jj in range(group_size):
+                j = t * group_size + jj
+                sg = s[rows].copy()
+                for c in range(len(cand)):
+                    sg[jj] = cand[c]
+                    errors[p, j, c] = group_error(Wg, sg, ag, symmetric)
+                e = errors[p, j]
+                best = cur[j]
+                for c in range(len(cand)):           # strictly better; the first in k order among equals
+                    if e[c] < e[best]:
+                        best = c
+                if follow is not None:
+                    best = int(follow[p, j])
+                trace[p, j] = best
+                cur[j] = best
+                s[j] = cand[best]
+    return s, trace, errors
+
+
+# ---------------------------------------------------------------------------
 # Step 4: offline pack of Quantize(diag(s*) W)
 # [concept] 推理时的等效实现 (W_quantized = Quantize(diag(s*) W), s* kept as
 # metadata); [adr] Consequences (two 4-bit weights per byte).

@@ -385,3 +385,62 @@ def check_act_stats_stream_matches_single_shot(orc):
 
 
 ALL_CHECKS += [check_act_stats_max_closed_forms, check_act_stats_stream_matches_single_shot]
+
+
+# ---------------------------------------------------------------- the ADR's greedy search
+def check_greedy_group_error_bruteforce(orc, seed=12):
+    """The greedy's objective written out element by element with the
+    nearest-code quantiser: sum_j a_j sum_n (w'hat_jn / s_j - w_jn)^2."""
+    rng = _rng(seed)
+    for sym in (False, True):
+        Wg = (rng.standard_normal((8, 5)) * 0.02).astype(F32)
+        s = np.array([1, 2, 0.5, 1, 4, 1, 0.25, 1], dtype=F32)
+        a = rng.uniform(0.1, 3.0, 8)
+        Wh = _scaled_quant_dequant_bruteforce(Wg, s, 8, sym, orc)
+        want = 0.0
+        for j in range(8):
+            for n in range(5):
+                d = Wh[j, n] - float(Wg[j, n])
+                want += float(a[j]) * d * d
+        got = orc.group_error(Wg, s, a, sym)
+        assert abs(got - want) <= 1e-12 * want, (got, want)
+
+
+def check_greedy_decisions(orc, seed=13):
+    """Every decision is the argmin of the group error over the candidates
+    (recomputed here independently), never worse than keeping the current
+    scale; grid = powers of two around 1; a salient channel ends above 1."""
+    rng = _rng(seed)
+    cand = orc.greedy_candidates()
+    assert len(cand) == 20 and cand[10] == 1.0 and np.all(cand[1:] == 2 * cand[:-1])
+    W = (rng.standard_normal((16, 12)) * 0.02).astype(F32)
+    a = rng.uniform(0.5, 1.5, 16)
+    a[5] = 60.0                     # salient channel ...
+    W[5] *= 0.1                     # ... whose weights sit far below the group max
+    W[2] = 0.0                      # every candidate gives the same error: the scale stays 1
+    for sym in (False, True):
+        s, trace, errors = orc.greedy_search(W, a, group_size=8, symmetric=sym, passes=2)
+        # replay: each decision against errors recomputed from the running s
+        cur = np.ones(16, dtype=F32)
+        for p in range(2):
+            for j in range(16):
+                t = j // 8
+                rows = slice(8 * t, 8 * t + 8)
+                e = []
+                for c in cand:
+                    trial = cur[rows].copy()
+                    trial[j - 8 * t] = c
+                    e.append(orc.group_error(W[rows], trial, a[rows], sym))
+                e = np.array(e)
+                np.testing.assert_allclose(errors[p, j], e, rtol=1e-12)
+                k = int(trace[p, j])
+                prev = int(np.flatnonzero(cand == cur[j])[0])
+                assert e[k] == e.min() and e[k] <= e[prev]
+                assert k == prev or e[k] < e[prev]
+                cur[j] = cand[k]
+        assert np.array_equal(cur, s)
+        assert s[5] > 1.0 and s[2] == 1.0
+        assert orc.group_error(W[:8], s[:8], a[:8], sym) < orc.group_error(W[:8], np.ones(8, F32), a[:8], sym)
+
+
+ALL_CHECKS += [check_greedy_group_error_bruteforce, check_greedy_decisions]

@@ -44,6 +44,13 @@ MUTANTS = [
     ("max_stat_no_abs", "return np.abs(X64).max(axis=0).astype(F32)", "return X64.max(axis=0).astype(F32)"),
     ("stream_mean_of_batch_means", "total = part if total is None else total + part\n        rows += X64.shape[0]",
      "part = part / X64.shape[0]\n        total = part if total is None else total + part\n        rows += 1"),
+    ("greedy_weight_squared", "return float((np.asarray(a, dtype=np.float64)[:, None] * D * D).sum())",
+     "return float((np.asarray(a, dtype=np.float64)[:, None] ** 2 * D * D).sum())"),
+    ("greedy_error_in_scaled_space", "D = What.astype(np.float64) / s.astype(np.float64)[:, None] - Wg.astype(np.float64)",
+     "D = What.astype(np.float64) - (Wg * s[:, None]).astype(np.float64)"),
+    ("greedy_keeps_last_of_equals", "if e[c] < e[best]:", "if e[c] <= e[best]:"),
+    ("greedy_grid_off_by_one", "return np.array([2.0 ** k for k in range(k_min, k_min + count)], dtype=F32)",
+     "return np.array([2.0 ** k for k in range(k_min + 1, k_min + count + 1)], dtype=F32)"),
     ("alpha_scaled_twice", "return np.power(a.astype(np.float64), np.float64(alpha)).astype(F32)",
      "return np.power(a.astype(np.float64), np.float64(2 * alpha)).astype(F32)"),
 ]
