@@ -245,6 +245,38 @@ AWQ_API awq_status awq_quantize_pack_searched(const void* W, int64_t D_in, int64
                                               void* scales, void* zeros, awq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The ADR's second search: per-group coordinate greedy over power-of-two
+ * channel scales ("009. AWQ Integration", 关键设计 1-3).
+ *
+ * Groups of cfg->group_size input rows are independent.  Starting from
+ * s = 1, for each pass and each channel j of a group in index order, every
+ * candidate 2^k (k = k_min .. k_min + n_cand - 1) is tried for s_j with the
+ * group's other scales fixed, and the group's activation-weighted
+ * reconstruction error
+ *     E = sum_i a_i sum_n (w'hat_in / s_i - w_in)^2,  w' = w s,
+ * is evaluated with the pack's own quantiser (cfg); s_j moves to the best
+ * candidate when that is strictly better than its current value (the first
+ * in k order among equals).  The ADR's defaults: passes 3, 20 candidates
+ * centred on 1 (k_min = -10).
+ *
+ *   W, D_in, D_out   device, bf16 [D_in, D_out] (D_in a multiple of group_size, D_out of 8)
+ *   mean_abs         device, fp32 [D_in]: the channel weights a_i (awq_act_stats)
+ *   s_out            device, fp32 [D_in], written: the final scales (powers of two)
+ *   trace            device, int32 [passes, D_in] or NULL: the candidate index chosen at each step
+ *   errors           device, fp64 [passes, D_in, n_cand] or NULL: E of every candidate at each step
+ *   ws               device workspace of awq_greedy_workspace_size() bytes
+ * Per-column errors are fp32; a group's candidates are compared on their
+ * error changes against the part common to all of them, summed in a fixed
+ * order in fp64, so the result is deterministic.  Constraints: 1 <= passes
+ * <= 16, 1 <= n_cand <= 24, 1 among the candidates.  s_out can be passed to
+ * awq_quantize_pack.  A step above the fp16 range sets AWQ_ERR_RANGE in ws.
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_greedy_workspace_size(int64_t D_in, int64_t D_out, const awq_cfg* cfg, size_t* bytes);
+AWQ_API awq_status awq_greedy_search(const void* W, const float* mean_abs, int64_t D_in, int64_t D_out,
+                                     const awq_cfg* cfg, int32_t passes, int32_t k_min, int32_t n_cand, float* s_out,
+                                     int32_t* trace, double* errors, void* ws, size_t ws_bytes, awq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * After the path: the W4A16 product on the packed layer.
  *
  * "AWQ (Activation-aware Weight Quantization)", 推理时的等效实现: the layer is

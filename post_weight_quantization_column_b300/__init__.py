@@ -64,6 +64,9 @@ _SIGS = {
                           ctypes.c_int),
     "awq_quantize_pack_searched": ([_vp, _c_i64, _c_i64, _c_i32, ctypes.POINTER(awq_cfg), _vp, _c_sz, _vp, _vp,
                                     _vp, _vp, _vp, _vp], ctypes.c_int),
+    "awq_greedy_workspace_size": ([_c_i64, _c_i64, ctypes.POINTER(awq_cfg), ctypes.POINTER(_c_sz)], ctypes.c_int),
+    "awq_greedy_search": ([_vp, _vp, _c_i64, _c_i64, ctypes.POINTER(awq_cfg), _c_i32, _c_i32, _c_i32, _vp, _vp, _vp,
+                           _vp, _c_sz, _vp], ctypes.c_int),
     "awq_w4a16_matmul": ([_vp, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp, ctypes.POINTER(awq_cfg), _vp, _vp, _c_sz,
                           _vp], ctypes.c_int),
     "awq_selftest_gemm_bf16": ([_vp, _vp, _c_i32, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_sz, _vp], ctypes.c_int),
@@ -314,6 +317,32 @@ def quantize_pack_searched(W: torch.Tensor, result: SearchResult, group_size: in
                                             _ptr(scales), _ptr(zeros), _stream_handle(stream)),
            "awq_quantize_pack_searched")
     return qweight, scales, zeros
+
+
+# ---------------------------------------------------------------------- the ADR's greedy search
+def greedy_search(W: torch.Tensor, mean_abs: torch.Tensor, group_size: int = 128, symmetric: bool = False,
+                  passes: int = 3, k_min: int = -10, n_cand: int = 20, trace: bool = False, errors: bool = False,
+                  stream=None, check: bool = True):
+    """Per-group coordinate greedy over 2^k channel scales -> s fp32 [D_in] (and, when asked,
+    the chosen candidate per step [passes, D_in] and every evaluated error [passes, D_in, n_cand])."""
+    _need(W, torch.bfloat16, "W")
+    _need(mean_abs, torch.float32, "mean_abs")
+    D_in, D_out = W.shape
+    dev = W.device
+    cfg = make_cfg(group_size, symmetric)
+    n = ctypes.c_size_t(0)
+    _check(lib().awq_greedy_workspace_size(D_in, D_out, ctypes.byref(cfg), ctypes.byref(n)),
+           "awq_greedy_workspace_size")
+    ws = _alloc_ws(n.value, dev)
+    s = torch.empty(D_in, dtype=torch.float32, device=dev)
+    tr = torch.empty(passes, D_in, dtype=torch.int32, device=dev) if trace else None
+    er = torch.empty(passes, D_in, n_cand, dtype=torch.float64, device=dev) if errors else None
+    _check(lib().awq_greedy_search(_ptr(W), _ptr(mean_abs), D_in, D_out, ctypes.byref(cfg), passes, k_min, n_cand,
+                                   _ptr(s), _ptr(tr), _ptr(er), _ptr(ws), ws.numel(), _stream_handle(stream)),
+           "awq_greedy_search")
+    if check:
+        check_workspace(ws, "awq_greedy_search (device)", stream)
+    return s, tr, er
 
 
 # ---------------------------------------------------------------------- after the path

@@ -455,6 +455,67 @@ awq_status awq_quantize_pack_searched(const void* W, int64_t D_in, int64_t D_out
                                         qweight, scales, zeros, cs));
 }
 
+// ------------------------------------------------------------------ the adr's greedy search
+namespace {
+// greedy workspace: header | current candidate index [D_in] int32 |
+// partials [T][slices][kMaxGreedyCand + 1] fp32 | tickets [T]
+struct GreedyLayout {
+  size_t idx, partial, tickets, total;
+};
+GreedyLayout greedy_layout(int64_t D_in, int64_t D_out, int group_size) {
+  GreedyLayout L;
+  const int64_t T = D_in / group_size;
+  L.idx = kHeaderBytes;
+  L.partial = L.idx + align_up(static_cast<size_t>(D_in) * 4, 256);
+  L.tickets = L.partial + align_up(static_cast<size_t>(T) * greedy_slices(D_out) * (kMaxGreedyCand + 1) * 4, 256);
+  L.total = L.tickets + align_up(static_cast<size_t>(T) * 4, 256);
+  return L;
+}
+awq_status validate_greedy(int64_t D_in, int64_t D_out, const awq_cfg* cfg, int32_t passes, int32_t k_min,
+                           int32_t n_cand) {
+  awq_status st = validate_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (D_in < 0 || D_out < 0 || D_in % cfg->group_size != 0 || D_out % 8 != 0) return AWQ_ERR_SHAPE;
+  if (D_in > INT32_MAX || D_out > INT32_MAX || D_in / cfg->group_size > 65535) return AWQ_ERR_SHAPE;
+  if (passes < 1 || passes > 16 || n_cand < 1 || n_cand > kMaxGreedyCand) return AWQ_ERR_INVALID_ARG;
+  if (k_min > 0 || k_min + n_cand <= 0 || k_min < -60 || k_min + n_cand > 60) return AWQ_ERR_INVALID_ARG;
+  return AWQ_OK;
+}
+}  // namespace
+
+awq_status awq_greedy_workspace_size(int64_t D_in, int64_t D_out, const awq_cfg* cfg, size_t* bytes) {
+  if (!bytes) return AWQ_ERR_INVALID_ARG;
+  awq_status st = validate_greedy(D_in, D_out, cfg, 1, -10, 20);
+  if (st != AWQ_OK) return st;
+  *bytes = greedy_layout(D_in, D_out, cfg->group_size).total;
+  return AWQ_OK;
+}
+
+awq_status awq_greedy_search(const void* W, const float* mean_abs, int64_t D_in, int64_t D_out, const awq_cfg* cfg,
+                             int32_t passes, int32_t k_min, int32_t n_cand, float* s_out, int32_t* trace,
+                             double* errors, void* ws, size_t ws_bytes, awq_stream_t stream) {
+  awq_status st = validate_greedy(D_in, D_out, cfg, passes, k_min, n_cand);
+  if (st != AWQ_OK) return st;
+  if (D_in == 0 || D_out == 0) return AWQ_OK;
+  if (!W || !mean_abs || !s_out || !ws) return AWQ_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(mean_abs, 4) || !aligned(s_out, 4) || (trace && !aligned(trace, 4)) ||
+      (errors && !aligned(errors, 8)) || !aligned(ws, 256))
+    return AWQ_ERR_ALIGNMENT;
+  const GreedyLayout L = greedy_layout(D_in, D_out, cfg->group_size);
+  if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
+  st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  if (cudaMemsetAsync(ws, 0, kHeaderBytes, cs) != cudaSuccess) return AWQ_ERR_CUDA;
+  if (cudaMemsetAsync(base + L.tickets, 0, L.total - L.tickets, cs) != cudaSuccess) return AWQ_ERR_CUDA;
+  ProfScope prof("greedy", cs);
+  return from_cuda(launch_greedy(W, mean_abs, D_in, D_out, cfg->group_size, cfg->symmetric, passes, k_min, n_cand,
+                                 s_out, reinterpret_cast<int*>(base + L.idx), reinterpret_cast<float*>(base + L.partial),
+                                 reinterpret_cast<unsigned int*>(base + L.tickets), trace, errors, status_word(ws),
+                                 cs));
+}
+
 // ------------------------------------------------------------------ W4A16 product
 awq_status awq_w4a16_matmul(const void* X, int64_t M, int64_t D_in, int64_t D_out, const uint8_t* qweight,
                             const void* scales, const void* zeros, const float* s, const awq_cfg* cfg, void* Y,

@@ -82,6 +82,13 @@ cudaError_t launch_gemm_store(PFN_cuTensorMapEncodeTiled_v12000 encode, const vo
 int search_fused_m_tiles(int64_t N);
 // CTA pairs that fit on the device at once (occupancy query).
 cudaError_t search_fused_max_pairs(int* pairs);
+// The adr's per-group coordinate greedy over power-of-two scales 2^k,
+// k = k_min .. k_min + ncand - 1 (ncand <= kMaxGreedyCand).
+constexpr int kMaxGreedyCand = 24;
+int64_t greedy_slices(int64_t D_out);
+cudaError_t launch_greedy(const void* W, const float* a, int64_t D_in, int64_t D_out, int group_size, int symmetric,
+                          int passes, int k_min, int ncand, float* s_cur, int* cur_idx, float* partial,
+                          unsigned int* tickets, int* trace, double* errors, uint32_t* status, cudaStream_t stream);
 // W4A16 product Y = (X diag(1/s)) Dequant(qweight) on CTA pairs (s may be null).
 cudaError_t w4a16_max_pairs(int* pairs);
 cudaError_t launch_w4a16(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, int64_t M, int64_t D_in,

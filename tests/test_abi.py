@@ -122,6 +122,13 @@ def test_calls_validate_before_cuda(L):
     assert L.awq_act_stats_accumulate(fake, 8, 256, 256, None, None, fake, 1 << 20, None) == 1
     assert L.awq_act_stats_accumulate(fake, 8, 256, 256, ctypes.c_void_p(0x1004), None, fake, 1 << 20, None) == 3
     assert L.awq_act_stats_finalize(fake, 0, 256, fake, None) == 2
+    # greedy search: 1 not among the candidates, too many candidates, no passes, ragged D_out
+    gs = L.awq_greedy_search
+    assert gs(fake, fake, 256, 256, ctypes.byref(cfg), 3, 1, 20, fake, None, None, fake, 1 << 30, None) == 1
+    assert gs(fake, fake, 256, 256, ctypes.byref(cfg), 3, -10, 25, fake, None, None, fake, 1 << 30, None) == 1
+    assert gs(fake, fake, 256, 256, ctypes.byref(cfg), 0, -10, 20, fake, None, None, fake, 1 << 30, None) == 1
+    assert gs(fake, fake, 256, 260, ctypes.byref(cfg), 3, -10, 20, fake, None, None, fake, 1 << 30, None) == 2
+    assert gs(fake, fake, 256, 256, ctypes.byref(cfg), 3, -10, 20, fake, None, None, fake, 256, None) == 4
     # W4A16 product: D_in not a multiple of 64, D_out not a multiple of 16,
     # misaligned Y, workspace too small; no rows is a no-op
     mm = L.awq_w4a16_matmul
