@@ -471,6 +471,23 @@ def run_ours(args, world, rank, local):
               "ms": y_ms, "tflops": y_tf, "bound": "tensor", "peak": peaks["bf16_tflops"],
               "frac": y_tf / peaks["bf16_tflops"], "timing": "median of 10 launches, L2 flushed before each"}
         del Y
+
+    # ---- the adr's greedy search on the same layer (separate from the step)
+    gr = None
+    g_ev = []
+    for i in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush_l2()
+        e0.record()
+        awq.greedy_search(Wd, a_buf, g, sym, check=False)
+        e1.record()
+        g_ev.append((e0, e1))
+    torch.cuda.synchronize()
+    g_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in g_ev[1:])[0], world)
+    evals = 3.0 * Di * 20 * Do
+    gr = {"workload": f"adr greedy: 3 passes x 20 power-of-two candidates, D_in={Di} D_out={Do} g={g}",
+          "ms": g_ms, "candidate_column_evaluations": evals, "evals_per_s": evals / (g_ms * 1e-3),
+          "launches": 3 * g + 1, "timing": "best of 2 after one warm-up, L2 flushed before each"}
     for ws, nm in ((ws_s, "act_stats"), (ws_q, "search")):
         awq.check_workspace(ws, nm)
 
@@ -493,6 +510,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": int(launches),
         "clocks": clocks,
         "w4a16": w4,
+        "adr_greedy": gr,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         Xf, Wf = synth.bf16_to_f32(X), synth.bf16_to_f32(W)

@@ -12,9 +12,10 @@
 // forms its column's range without channel j, the error of the other rows
 // under the step / zero of that range, and then for each candidate only
 // the term of channel j -- unless the scaled channel widens the range, in
-// which case it re-sums the column under the new step / zero.  Codes use the
-// IEEE quotient w'/step as the oracle defines them (s is a power of two, so
-// w s and step / s are exact).  Column errors are summed in a fixed order
+// which case it re-sums the column under the new step / zero.  Codes are
+// rint of the IEEE quotient w'/step as the oracle defines them, formed as
+// w' * (1/step) and redone with the division within 8e-6 of a half step (s
+// is a power of two, so w s and step / s are exact).  Column errors are summed in a fixed order
 // (a warp tree, then the warps in order), the slices of a group in slice
 // order in fp64 by the last CTA of the group to finish (ticket counter),
 // which also takes the decision and updates the scale.
@@ -34,7 +35,13 @@ struct Range {
 
 struct Quant {
   float step, zero;  // zero: the asymmetric zero point (0 for symmetric codes)
+  float inv;         // RN(1 / step) (0 for a zero step)
 };
+
+// Within this distance of a half step the reciprocal product and the IEEE
+// quotient can round differently: |w'/step| <= 15 (1 + 2^-11) here, where the
+// product is within 2e-6 of the quotient.
+constexpr float kTieGuard = 0.5f - 8.0e-6f;
 
 template <bool SYM>
 __device__ __forceinline__ Quant quant_of(Range r, uint32_t* status) {
@@ -47,22 +54,58 @@ __device__ __forceinline__ Quant quant_of(Range r, uint32_t* status) {
   }
   q.step = sc;
   q.zero = (!SYM && sc != 0.f) ? fminf(fmaxf(rintf(__fdiv_rn(-r.lo, sc)), 0.f), 15.f) : 0.f;
+  q.inv = sc != 0.f ? __frcp_rn(sc) : 0.f;
   return q;
 }
 
-// a * (w'hat / s - w)^2 for one weight w with scale s (a power of two).
-template <bool SYM>
-__device__ __forceinline__ float term(float w, float s, float a, Quant q) {
+// a * (w'hat / s - w)^2 for one weight w with scale s and rs = 1/s (powers of
+// two).  The fast form takes rint(w' * (1/step)) and raises `dev` to the
+// distance of that product from its rounding; where dev ends above the tie
+// guard the caller redoes the column with the exact form (rint of the IEEE
+// quotient).
+template <bool SYM, bool EXACT>
+__device__ __forceinline__ float term(float w, float s, float rs, float a, Quant q, float& dev) {
   float d;
   if (q.step == 0.f) {
     d = -w;
   } else {
     const float wp = w * s;  // exact
-    const float t = rintf(__fdiv_rn(wp, q.step));
+    float t;
+    if (EXACT) {
+      t = rintf(__fdiv_rn(wp, q.step));
+    } else {
+      const float tq = wp * q.inv;
+      t = rintf(tq);
+      dev = fmaxf(dev, fabsf(tq - t));
+    }
     const float c = SYM ? fminf(fmaxf(t, -7.f), 7.f) : fminf(fmaxf(t + q.zero, 0.f), 15.f) - q.zero;
-    d = fmaf(c, q.step / s, -w);  // (code - zero) * step / s exact; one rounding of the difference
+    d = fmaf(c, q.step * rs, -w);  // (code - zero) * step / s exact; one rounding of the difference
   }
   return a * (d * d);
+}
+
+// sum over the group's rows of one column (row jj zeroed with weight 0)
+template <int GS, bool SYM>
+__device__ __forceinline__ float column_error(const __nv_bfloat16 (*wt)[128], const float* ss, const float* sr,
+                                              const float* sa, int t, Quant q) {
+  // four interleaved partial sums (rows i mod 4), added in a fixed order
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, dev[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+  for (int i = 0; i < GS; i += 4) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      acc[u] += term<SYM, false>(__bfloat162float(wt[i + u][t]), ss[i + u], sr[i + u], sa[i + u], q, dev[u]);
+  }
+  if (fmaxf(fmaxf(dev[0], dev[1]), fmaxf(dev[2], dev[3])) > kTieGuard) {
+    float d = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] = 0.f;
+    for (int i = 0; i < GS; i += 4)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        acc[u] += term<SYM, true>(__bfloat162float(wt[i + u][t]), ss[i + u], sr[i + u], sa[i + u], q, d);
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 template <bool SYM>
@@ -84,7 +127,7 @@ __global__ void __launch_bounds__(kGreedyCols)
                        double* __restrict__ errors, int64_t D_in, uint32_t* status) {
   extern __shared__ __align__(16) uint8_t dyn[];
   __nv_bfloat16 (*wt)[kGreedyCols] = reinterpret_cast<__nv_bfloat16 (*)[kGreedyCols]>(dyn);  // [GS][128]
-  __shared__ float sa[GS], ss[GS];
+  __shared__ float sa[GS], ss[GS], sr[GS];
   // per column: the error change of each candidate against the common part
   // (row kMaxGreedyCand: the common part itself, the other rows' error under
   // the range without channel jj)
@@ -110,10 +153,15 @@ __global__ void __launch_bounds__(kGreedyCols)
     *reinterpret_cast<uint4*>(&wt[i][c8]) = x;
   }
   for (int i = t; i < GS; i += kGreedyCols) {
-    sa[i] = a[row0 + i];
+    sa[i] = i == jj ? 0.f : a[row0 + i];  // channel jj's own term is added per candidate
     ss[i] = s_cur[row0 + i];
+    sr[i] = 1.f / ss[i];  // exact: a power of two
   }
   __syncthreads();
+  // each thread reads only its own column: take channel jj's weight and leave
+  // a zero in its place (a zero weight changes no range and adds no error)
+  const float wj = __bfloat162float(wt[jj][t]);
+  wt[jj][t] = __float2bfloat16(0.f);
 
   for (int c = 0; c <= kMaxGreedyCand; ++c) errs[c][t] = 0.f;
   if (active) {
@@ -121,25 +169,21 @@ __global__ void __launch_bounds__(kGreedyCols)
     Range ex;
     ex.lo = 0.f;
     ex.hi = 0.f;
-    for (int i = 0; i < GS; ++i)
-      if (i != jj) ex = widen<SYM>(ex, __bfloat162float(wt[i][t]) * ss[i]);
+#pragma unroll 8
+    for (int i = 0; i < GS; ++i) ex = widen<SYM>(ex, __bfloat162float(wt[i][t]) * ss[i]);
     const Quant qb = quant_of<SYM>(ex, status);
-    float base = 0.f;
-    for (int i = 0; i < GS; ++i)
-      if (i != jj) base += term<SYM>(__bfloat162float(wt[i][t]), ss[i], sa[i], qb);
-    const float wj = __bfloat162float(wt[jj][t]);
-    const float aj = sa[jj];
+    const float base = column_error<GS, SYM>(wt, ss, sr, sa, t, qb);
+    const float aj = a[row0 + jj];
 #pragma unroll 1
     for (int c = 0; c < ncand; ++c) {
       const float sc = ldexpf(1.f, k_min + c);
       const Quant q = quant_of<SYM>(widen<SYM>(ex, wj * sc), status);
       float e = 0.f;  // change of the other rows' error
-      if (q.step != qb.step || q.zero != qb.zero) {
-        for (int i = 0; i < GS; ++i)
-          if (i != jj) e += term<SYM>(__bfloat162float(wt[i][t]), ss[i], sa[i], q);
-        e -= base;
-      }
-      errs[c][t] = e + term<SYM>(wj, sc, aj, q);
+      if (q.step != qb.step || q.zero != qb.zero) e = column_error<GS, SYM>(wt, ss, sr, sa, t, q) - base;
+      float dev = 0.f;
+      float own = term<SYM, false>(wj, sc, 1.f / sc, aj, q, dev);
+      if (dev > kTieGuard) own = term<SYM, true>(wj, sc, 1.f / sc, aj, q, dev);
+      errs[c][t] = e + own;
     }
     errs[kMaxGreedyCand][t] = base;
   }
@@ -170,10 +214,20 @@ __global__ void __launch_bounds__(kGreedyCols)
     // each summed over the slices in order; the decision compares changes
     const float* pg = partial + static_cast<int64_t>(g) * slices * (kMaxGreedyCand + 1);
     double e = 0.0, common = 0.0;
-    if (t < ncand)
-      for (int sl = 0; sl < slices; ++sl) e += static_cast<double>(pg[sl * (kMaxGreedyCand + 1) + t]);
-    if (errors)
-      for (int sl = 0; sl < slices; ++sl) common += static_cast<double>(pg[sl * (kMaxGreedyCand + 1) + kMaxGreedyCand]);
+    for (int s0 = 0; s0 < slices; s0 += 16) {
+      float v[16], b[16];  // 16 slices' loads in flight, added in slice order
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const bool in = s0 + i < slices;
+        v[i] = in && t < ncand ? pg[(s0 + i) * (kMaxGreedyCand + 1) + t] : 0.f;
+        b[i] = in && errors ? pg[(s0 + i) * (kMaxGreedyCand + 1) + kMaxGreedyCand] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        e += static_cast<double>(v[i]);
+        common += static_cast<double>(b[i]);
+      }
+    }
     const int64_t j = row0 + jj;
     if (errors && t < ncand) errors[(static_cast<int64_t>(pass) * D_in + j) * ncand + t] = common + e;
     // strictly better than the current scale; the first in k order among equals
