@@ -124,6 +124,23 @@ def scales(mean_abs: np.ndarray, alpha: float, act_floor: float = 1e-4) -> np.nd
     return np.power(a.astype(np.float64), np.float64(alpha)).astype(F32)
 
 
+def closed_form_scales(W: np.ndarray, mean_abs: np.ndarray, alpha: float = 0.5,
+                       act_floor: float = 1e-4) -> np.ndarray:
+    """The closed-form scale of [aiqz] section 3: s_i = (E|X_i|)^alpha / mean_j |W_ij|,
+    one value per input channel i (row i of W [D_in, D_out]), alpha = 0.5 by
+    default.  Readings: E|X_i| is the floored statistic as for the grid
+    search; mean_j |W_ij| is summed in float64; the quotient is formed in
+    float64 and rounded once to float32; a row of zeros gets s = 1 (its
+    weights quantise to zero whatever s is)."""
+    W64 = np.asarray(W, dtype=F32).astype(np.float64)
+    den = np.abs(W64).sum(axis=1) / W64.shape[1]
+    stat = np.maximum(np.asarray(mean_abs, dtype=np.float32), np.float32(act_floor))   # floored as in scales()
+    num = np.power(stat.astype(np.float64), np.float64(alpha))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s = np.where(den > 0, num / np.where(den > 0, den, 1.0), 1.0)
+    return s.astype(F32)
+
+
 # ---------------------------------------------------------------------------
 # Step 2b: per-group b-bit quantisation of W' = diag(s) W
 # [concept] 技术原理 - 量化数学基础 (absmax step, round, clamp, dequant);

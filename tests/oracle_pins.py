@@ -444,3 +444,20 @@ def check_greedy_decisions(orc, seed=13):
 
 
 ALL_CHECKS += [check_greedy_group_error_bruteforce, check_greedy_decisions]
+
+
+# ---------------------------------------------------------------- closed-form scale
+def check_closed_form_scales(orc):
+    """Rows of constant magnitude c give mean |W_i| = c; alpha = 0 gives 1/c;
+    alpha = 1/2 the square root over c; a zero row gets 1; the floor applies
+    to the statistic."""
+    W = np.array([[0.5, -0.5, 0.5, -0.5], [2.0, 2.0, -2.0, 2.0], [0.0, 0.0, 0.0, 0.0],
+                  [0.25, -0.75, 0.0, 0.5]], dtype=F32)
+    a = np.array([4.0, 9.0, 3.0, 0.0], dtype=F32)
+    assert np.array_equal(orc.closed_form_scales(W, a, 0.0), np.array([2.0, 0.5, 1.0, F32(1 / 0.375)], dtype=F32))
+    floored = np.sqrt(np.float64(F32(1e-4)))  # the statistic's floor is the fp32 value of 1e-4
+    assert np.array_equal(orc.closed_form_scales(W, a, 0.5), np.array([4.0, 1.5, 1.0, F32(floored / 0.375)], dtype=F32))
+    assert np.array_equal(orc.closed_form_scales(W, a, 1.0)[:2], np.array([8.0, 4.5], dtype=F32))
+
+
+ALL_CHECKS.append(check_closed_form_scales)

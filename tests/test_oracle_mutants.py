@@ -51,6 +51,11 @@ MUTANTS = [
     ("greedy_keeps_last_of_equals", "if e[c] < e[best]:", "if e[c] <= e[best]:"),
     ("greedy_grid_off_by_one", "return np.array([2.0 ** k for k in range(k_min, k_min + count)], dtype=F32)",
      "return np.array([2.0 ** k for k in range(k_min + 1, k_min + count + 1)], dtype=F32)"),
+    ("closed_form_mean_over_rows", "den = np.abs(W64).sum(axis=1) / W64.shape[1]",
+     "den = np.abs(W64).sum(axis=0)[: W64.shape[0]] / W64.shape[0]"),
+    ("closed_form_no_abs", "den = np.abs(W64).sum(axis=1) / W64.shape[1]", "den = np.abs(W64.sum(axis=1)) / W64.shape[1]"),
+    ("closed_form_alpha_on_both", "s = np.where(den > 0, num / np.where(den > 0, den, 1.0), 1.0)",
+     "s = np.where(den > 0, num / np.power(np.where(den > 0, den, 1.0), alpha), 1.0)"),
     ("alpha_scaled_twice", "return np.power(a.astype(np.float64), np.float64(alpha)).astype(F32)",
      "return np.power(a.astype(np.float64), np.float64(2 * alpha)).astype(F32)"),
 ]
