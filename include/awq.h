@@ -245,6 +245,21 @@ AWQ_API awq_status awq_quantize_pack_searched(const void* W, int64_t D_in, int64
                                               void* scales, void* zeros, awq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The closed-form scale (aiqz.cc article "awq-activation-aware-quantization",
+ * section 3): one scale per input channel without a search,
+ *     s_i = (E|X_i|)^alpha / mean_j |W_ij|,   alpha in [0, 1] (0.5 by default).
+ *
+ *   W, D_in, D_out   device, bf16 [D_in, D_out] (D_out a multiple of 8); row i = channel i
+ *   mean_abs         device, fp32 [D_in]: E|X_i| (awq_act_stats), floored at cfg->act_floor
+ *   s_out            device, fp32 [D_in], written
+ * mean_j |W_ij| is summed in fp64 (exact for rows spanning up to ~30
+ * binades), the quotient formed in fp64 and rounded once to fp32; a row of
+ * zeros gets s = 1.  s_out can be passed to awq_quantize_pack.
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_closed_form_scales(const void* W, int64_t D_in, int64_t D_out, const float* mean_abs,
+                                          double alpha, const awq_cfg* cfg, float* s_out, awq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * The ADR's second search: per-group coordinate greedy over power-of-two
  * channel scales ("009. AWQ Integration", 关键设计 1-3).
  *

@@ -64,6 +64,8 @@ _SIGS = {
                           ctypes.c_int),
     "awq_quantize_pack_searched": ([_vp, _c_i64, _c_i64, _c_i32, ctypes.POINTER(awq_cfg), _vp, _c_sz, _vp, _vp,
                                     _vp, _vp, _vp, _vp], ctypes.c_int),
+    "awq_closed_form_scales": ([_vp, _c_i64, _c_i64, _vp, ctypes.c_double, ctypes.POINTER(awq_cfg), _vp, _vp],
+                               ctypes.c_int),
     "awq_greedy_workspace_size": ([_c_i64, _c_i64, ctypes.POINTER(awq_cfg), ctypes.POINTER(_c_sz)], ctypes.c_int),
     "awq_greedy_search": ([_vp, _vp, _c_i64, _c_i64, ctypes.POINTER(awq_cfg), _c_i32, _c_i32, _c_i32, _vp, _vp, _vp,
                            _vp, _c_sz, _vp], ctypes.c_int),
@@ -317,6 +319,21 @@ def quantize_pack_searched(W: torch.Tensor, result: SearchResult, group_size: in
                                             _ptr(scales), _ptr(zeros), _stream_handle(stream)),
            "awq_quantize_pack_searched")
     return qweight, scales, zeros
+
+
+# ---------------------------------------------------------------------- closed-form scale
+def closed_form_scales(W: torch.Tensor, mean_abs: torch.Tensor, alpha: float = 0.5, act_floor: float = 1e-4,
+                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """s_i = (max(E|X_i|, floor))^alpha / mean_j |W_ij| -> fp32 [D_in] (a zero row gets 1)."""
+    _need(W, torch.bfloat16, "W")
+    _need(mean_abs, torch.float32, "mean_abs")
+    D_in, D_out = W.shape
+    if out is None:
+        out = torch.empty(D_in, dtype=torch.float32, device=W.device)
+    cfg = make_cfg(act_floor=act_floor)
+    _check(lib().awq_closed_form_scales(_ptr(W), D_in, D_out, _ptr(mean_abs), float(alpha), ctypes.byref(cfg),
+                                        _ptr(out), _stream_handle(stream)), "awq_closed_form_scales")
+    return out
 
 
 # ---------------------------------------------------------------------- the ADR's greedy search

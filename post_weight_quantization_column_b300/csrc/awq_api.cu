@@ -455,6 +455,23 @@ awq_status awq_quantize_pack_searched(const void* W, int64_t D_in, int64_t D_out
                                         qweight, scales, zeros, cs));
 }
 
+// ------------------------------------------------------------------ closed-form scale
+awq_status awq_closed_form_scales(const void* W, int64_t D_in, int64_t D_out, const float* mean_abs, double alpha,
+                                  const awq_cfg* cfg, float* s_out, awq_stream_t stream) {
+  awq_status st = validate_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (D_in < 0 || D_out < 0 || D_out % 8 != 0) return AWQ_ERR_SHAPE;
+  if (!(alpha >= 0.0 && alpha <= 1.0)) return AWQ_ERR_INVALID_ARG;
+  if (D_in == 0 || D_out == 0) return AWQ_OK;
+  if (!W || !mean_abs || !s_out) return AWQ_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(mean_abs, 4) || !aligned(s_out, 4)) return AWQ_ERR_ALIGNMENT;
+  st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  ProfScope prof("closed_form", cs);
+  return from_cuda(launch_closed_form(W, D_in, D_out, mean_abs, alpha, cfg->act_floor, s_out, cs));
+}
+
 // ------------------------------------------------------------------ the adr's greedy search
 namespace {
 // greedy workspace: header | current candidate index [D_in] int32 |

@@ -56,6 +56,9 @@ inline size_t qparam_floats(int G, int64_t T, int64_t D_out) {
 
 cudaError_t launch_scale_table(const float* mean_abs, int64_t D_in, const AlphaGrid& grid, int G, float act_floor,
                                float* s_tab, float* r_tab, uint32_t* status, cudaStream_t stream);
+// s_i = (max(a_i, floor))^alpha / mean_j |W_ij| (a zero row: 1).
+cudaError_t launch_closed_form(const void* W, int64_t D_in, int64_t D_out, const float* mean_abs, double alpha,
+                               float act_floor, float* s_out, cudaStream_t stream);
 cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in, int64_t D_out, int G,
                                 int group_size, int symmetric, float* qp, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_pack(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* W, const float* s, int64_t D_in,

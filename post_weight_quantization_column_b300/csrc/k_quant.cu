@@ -53,6 +53,48 @@ cudaError_t launch_scale_table(const float* mean_abs, int64_t D_in, const AlphaG
 
 // ------------------------------------------------------------------ group parameters
 // Exact step / zero of one (group, column) from the range of its scaled weights.
+// The closed-form scale of the aiqz.cc article (section 3):
+//   s_i = (E|X_i|)^alpha / mean_j |W_ij|
+// for input channel i (row i of W [D_in, D_out]).  One warp per row: 16-byte
+// loads along the row, |w| accumulated in fp64 (a sum of bf16 magnitudes is
+// exact in fp64 while the row spans at most ~30 binades, so the result does
+// not depend on the order), a fixed-order warp tree; the quotient in fp64,
+// rounded once to fp32.  The statistic is floored as for the grid search; a
+// row of zeros gets s = 1.
+__global__ void closed_form_kernel(const __nv_bfloat16* __restrict__ W, int64_t D_in, int64_t D_out,
+                                   const float* __restrict__ mean_abs, double alpha, float act_floor,
+                                   float* __restrict__ s_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (row >= D_in) return;
+  const __nv_bfloat16* wr = W + row * D_out;
+  double acc = 0.0;
+  for (int64_t c = static_cast<int64_t>(lane) * 8; c < D_out; c += 32 * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(wr + c);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc += static_cast<double>(__uint_as_float((u[k] << 16) & 0x7FFFFFFFu));
+      acc += static_cast<double>(__uint_as_float(u[k] & 0x7FFF0000u));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (lane == 0) {
+    const double den = acc / static_cast<double>(D_out);
+    const double a = static_cast<double>(fmaxf(mean_abs[row], act_floor));
+    s_out[row] = den > 0.0 ? static_cast<float>(pow(a, alpha) / den) : 1.f;
+  }
+}
+
+cudaError_t launch_closed_form(const void* W, int64_t D_in, int64_t D_out, const float* mean_abs, double alpha,
+                               float act_floor, float* s_out, cudaStream_t stream) {
+  constexpr int kRowsPerCta = 8;
+  closed_form_kernel<<<static_cast<unsigned>((D_in + kRowsPerCta - 1) / kRowsPerCta), kRowsPerCta * 32, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(W), D_in, D_out, mean_abs, alpha, act_floor, s_out);
+  return cudaGetLastError();
+}
+
 __device__ __forceinline__ QParam make_qparam(float lo, float hi, int symmetric, uint32_t* status) {
   QParam q;
   q.pad = 0.f;

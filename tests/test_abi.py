@@ -122,6 +122,9 @@ def test_calls_validate_before_cuda(L):
     assert L.awq_act_stats_accumulate(fake, 8, 256, 256, None, None, fake, 1 << 20, None) == 1
     assert L.awq_act_stats_accumulate(fake, 8, 256, 256, ctypes.c_void_p(0x1004), None, fake, 1 << 20, None) == 3
     assert L.awq_act_stats_finalize(fake, 0, 256, fake, None) == 2
+    # closed-form scale: alpha outside [0, 1], ragged D_out
+    assert L.awq_closed_form_scales(fake, 256, 256, fake, 1.5, ctypes.byref(cfg), fake, None) == 1
+    assert L.awq_closed_form_scales(fake, 256, 252, fake, 0.5, ctypes.byref(cfg), fake, None) == 2
     # greedy search: 1 not among the candidates, too many candidates, no passes, ragged D_out
     gs = L.awq_greedy_search
     assert gs(fake, fake, 256, 256, ctypes.byref(cfg), 3, 1, 20, fake, None, None, fake, 1 << 30, None) == 1
