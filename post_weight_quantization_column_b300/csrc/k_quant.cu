@@ -140,102 +140,115 @@ __device__ __forceinline__ float fmaxabs3(float a, float b, float c) {
 
 constexpr int kGpThreads = 128;   // one output column per thread
 constexpr int kGpCols = kGpThreads;
-constexpr int kMaxGpCandidates = 32;  // candidates per CTA (grid.z splits larger grids)
+constexpr int kMaxGpCandidates = 21;  // candidates per CTA, the default grid (grid.z splits larger grids)
+constexpr int kGpChunk = 64;          // rows of W staged per step (16 KB)
 
-// One CTA: one group of GS rows x 128 columns, up to 32 candidates.  The W tile
-// (GS x 128 bf16) and the group's scale rows sit in shared memory, the
-// scales as {s_k[r], s_k[r+1]} pairs so that one 8-byte broadcast load feeds
-// a packed multiply.  Thread t owns column t and keeps the running range of
-// all G candidates in registers: for each pair of rows it unpacks its two
-// weights once, then per candidate does w' = w s for both rows in one packed
-// multiply and a three-input min / max against the running range.
+// One CTA: one group of GS rows x 128 columns, up to 21 candidates.  The group
+// streams through shared memory in 64-row chunks (W chunk 16 KB, the chunk's
+// scale rows as {s_k[r], s_k[r+1]} pairs so that one 8-byte broadcast load
+// feeds a packed multiply).  Thread t owns column t and keeps the running
+// range of all candidates in registers: for each pair of rows it unpacks its
+// two weights once, then per candidate does w' = w s for both rows in one
+// packed multiply and a three-input min / max against the running range.
+// 22 KB of shared memory and <= 72 registers put 7 CTAs on an SM, so a
+// 4096 x 4096 layer's 1024 CTAs run in one wave.
 template <int GS>
-__global__ void __launch_bounds__(kGpThreads) group_params_kernel(const __nv_bfloat16* __restrict__ W,
+__global__ void __launch_bounds__(kGpThreads, 7) group_params_kernel(const __nv_bfloat16* __restrict__ W,
                                                                 const float* __restrict__ s_tab, int64_t D_in,
                                                                 int64_t D_out, int G, int symmetric,
                                                                 float* __restrict__ qp, uint32_t* status) {
   extern __shared__ __align__(16) uint8_t smem[];
-  __nv_bfloat16* wsh = reinterpret_cast<__nv_bfloat16*>(smem);     // [GS][128]
-  float2* ssh = reinterpret_cast<float2*>(smem + GS * kGpCols * 2);  // [GS/2][nk]
+  __nv_bfloat16* wsh = reinterpret_cast<__nv_bfloat16*>(smem);            // [64][128]
+  float2* ssh = reinterpret_cast<float2*>(smem + kGpChunk * kGpCols * 2);  // [32][nk]
   const int t = threadIdx.x;
   const int k0 = blockIdx.z * kMaxGpCandidates;
   const int nk = min(kMaxGpCandidates, G - k0);
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kGpCols;
   const int64_t grp = blockIdx.y;
-  const int64_t j0 = grp * GS;
-  bool bad = false;
-  {
-    // all of the thread's loads in flight before the first store
-    constexpr int kLoads = GS * (kGpCols / 8) / kGpThreads;
-    uint4 v[kLoads];
-#pragma unroll
-    for (int i = 0; i < kLoads; ++i) {
-      const int idx = t + i * kGpThreads;
-      const int64_t col = n0 + (idx & 15) * 8;
-      v[i] = col < D_out ? *reinterpret_cast<const uint4*>(W + (j0 + (idx >> 4)) * D_out + col)
-                         : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int i = 0; i < kLoads; ++i) {
-      const int idx = t + i * kGpThreads;
-      bad |= bf16x2_nonfinite(v[i].x) | bf16x2_nonfinite(v[i].y) | bf16x2_nonfinite(v[i].z) |
-             bf16x2_nonfinite(v[i].w);
-      *reinterpret_cast<uint4*>(wsh + (idx >> 4) * kGpCols + (idx & 15) * 8) = v[i];
-    }
-  }
-  {
-    // scale pairs, up to kMaxGpCandidates * GS/2 of them: all loads first
-    constexpr int kSLoads = kMaxGpCandidates * (GS / 2) / kGpThreads;
-    float2 sv[kSLoads];
-#pragma unroll
-    for (int i = 0; i < kSLoads; ++i) {
-      const int idx = t + i * kGpThreads;
-      const int k = idx / (GS / 2);
-      const int rp = idx - k * (GS / 2);
-      sv[i] = k < nk ? *reinterpret_cast<const float2*>(s_tab + static_cast<int64_t>(k0 + k) * D_in + j0 + 2 * rp)
-                     : make_float2(0.f, 0.f);
-    }
-#pragma unroll
-    for (int i = 0; i < kSLoads; ++i) {
-      const int idx = t + i * kGpThreads;
-      const int k = idx / (GS / 2);
-      const int rp = idx - k * (GS / 2);
-      if (k < nk) ssh[rp * nk + k] = sv[i];
-    }
-  }
-  if (bad && blockIdx.z == 0) set_error(status, AWQ_DEV_NONFINITE);
-  __syncthreads();
   const int64_t n = n0 + t;
-  if (n >= D_out) return;
+  bool bad = false;
 
   float lo[kMaxGpCandidates], hi[kMaxGpCandidates];
 #pragma unroll
   for (int k = 0; k < kMaxGpCandidates; ++k) lo[k] = hi[k] = 0.f;
-  const uint16_t* wcol = reinterpret_cast<const uint16_t*>(wsh) + t;
-#pragma unroll 2
-  for (int rp = 0; rp < GS / 2; ++rp) {
-    const float2 w2 = make_float2(__uint_as_float(static_cast<uint32_t>(wcol[(2 * rp) * kGpCols]) << 16),
-                                  __uint_as_float(static_cast<uint32_t>(wcol[(2 * rp + 1) * kGpCols]) << 16));
-    const float2* sp = ssh + rp * nk;
-    if (symmetric) {
+
+#pragma unroll 1
+  for (int c0 = 0; c0 < GS; c0 += kGpChunk) {
+    const int64_t j0 = grp * GS + c0;
+    if (c0 > 0) __syncthreads();  // every thread is done with the previous chunk
+    // the thread's W loads in two batches of four in flight (registers stay
+    // below the bound that puts 7 CTAs on an SM)
+    constexpr int kLoads = kGpChunk * (kGpCols / 8) / kGpThreads;
 #pragma unroll
-      for (int k = 0; k < kMaxGpCandidates; ++k) {
-        if (k < nk) {
-          const float2 p = __fmul2_rn(w2, sp[k]);
-          hi[k] = fmaxabs3(hi[k], p.x, p.y);
-        }
+    for (int b = 0; b < kLoads; b += 4) {
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = t + (b + i) * kGpThreads;
+        const int64_t col = n0 + (idx & 15) * 8;
+        v[i] = col < D_out ? *reinterpret_cast<const uint4*>(W + (j0 + (idx >> 4)) * D_out + col)
+                           : make_uint4(0u, 0u, 0u, 0u);
       }
-    } else {
 #pragma unroll
-      for (int k = 0; k < kMaxGpCandidates; ++k) {
-        if (k < nk) {
-          const float2 p = __fmul2_rn(w2, sp[k]);
-          lo[k] = fmin3(lo[k], p.x, p.y);
-          hi[k] = fmax3(hi[k], p.x, p.y);
+      for (int i = 0; i < 4; ++i) {
+        const int idx = t + (b + i) * kGpThreads;
+        bad |= bf16x2_nonfinite(v[i].x) | bf16x2_nonfinite(v[i].y) | bf16x2_nonfinite(v[i].z) |
+               bf16x2_nonfinite(v[i].w);
+        *reinterpret_cast<uint4*>(wsh + (idx >> 4) * kGpCols + (idx & 15) * 8) = v[i];
+      }
+    }
+    {
+      // scale pairs of the chunk, up to kMaxGpCandidates * 32 of them (rounded
+      // up to whole rounds of the CTA; the k < nk test skips the overhang)
+      constexpr int kSLoads = (kMaxGpCandidates * (kGpChunk / 2) + kGpThreads - 1) / kGpThreads;
+      float2 sv[kSLoads];
+#pragma unroll
+      for (int i = 0; i < kSLoads; ++i) {
+        const int idx = t + i * kGpThreads;
+        const int k = idx / (kGpChunk / 2);
+        const int rp = idx - k * (kGpChunk / 2);
+        sv[i] = k < nk ? *reinterpret_cast<const float2*>(s_tab + static_cast<int64_t>(k0 + k) * D_in + j0 + 2 * rp)
+                       : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < kSLoads; ++i) {
+        const int idx = t + i * kGpThreads;
+        const int k = idx / (kGpChunk / 2);
+        const int rp = idx - k * (kGpChunk / 2);
+        if (k < nk) ssh[rp * nk + k] = sv[i];
+      }
+    }
+    __syncthreads();
+    if (n < D_out) {
+      const uint16_t* wcol = reinterpret_cast<const uint16_t*>(wsh) + t;
+#pragma unroll 2
+      for (int rp = 0; rp < kGpChunk / 2; ++rp) {
+        const float2 w2 = make_float2(__uint_as_float(static_cast<uint32_t>(wcol[(2 * rp) * kGpCols]) << 16),
+                                      __uint_as_float(static_cast<uint32_t>(wcol[(2 * rp + 1) * kGpCols]) << 16));
+        const float2* sp = ssh + rp * nk;
+        if (symmetric) {
+#pragma unroll
+          for (int k = 0; k < kMaxGpCandidates; ++k) {
+            if (k < nk) {
+              const float2 p = __fmul2_rn(w2, sp[k]);
+              hi[k] = fmaxabs3(hi[k], p.x, p.y);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kMaxGpCandidates; ++k) {
+            if (k < nk) {
+              const float2 p = __fmul2_rn(w2, sp[k]);
+              lo[k] = fmin3(lo[k], p.x, p.y);
+              hi[k] = fmax3(hi[k], p.x, p.y);
+            }
+          }
         }
       }
     }
   }
+  if (bad && blockIdx.z == 0) set_error(status, AWQ_DEV_NONFINITE);
+  if (n >= D_out) return;
   const int64_t T = D_in / GS;
   const int64_t kstride = T * (D_out / kQChunkCols) * kQChunkFloats;
   float* dst0 = qp + k0 * kstride + (grp * (D_out / kQChunkCols) + n / kQChunkCols) * kQChunkFloats +
@@ -252,8 +265,8 @@ __global__ void __launch_bounds__(kGpThreads) group_params_kernel(const __nv_bfl
   }
 }
 
-static size_t group_params_smem(int GS) {
-  return static_cast<size_t>(GS) * kGpCols * 2 + static_cast<size_t>(GS / 2) * kMaxGpCandidates * 8;
+static size_t group_params_smem(int) {
+  return static_cast<size_t>(kGpChunk) * kGpCols * 2 + static_cast<size_t>(kGpChunk / 2) * kMaxGpCandidates * 8;
 }
 
 template <int GS>
