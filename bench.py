@@ -471,6 +471,24 @@ def run_ours(args, world, rank, local):
               "ms": y_ms, "tflops": y_tf, "bound": "tensor", "peak": peaks["bf16_tflops"],
               "frac": y_tf / peaks["bf16_tflops"], "timing": "median of 10 launches, L2 flushed before each"}
         del Y
+        # one row of X through the same packed layer: the decode path, bound by the code bytes
+        X1 = Xd[:1].contiguous()
+        Y1 = torch.empty(1, Do, dtype=torch.bfloat16, device=dev)
+        ws_1 = torch.empty(awq.w4a16_workspace_size(1, Di, Do), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            awq.w4a16_matmul(X1, *pk, res.s_star, g, out=Y1, ws=ws_1, check=False)
+        d_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+        for i in range(10):
+            flush_l2()
+            d_ev[i][0].record()
+            awq.w4a16_matmul(X1, *pk, res.s_star, g, out=Y1, ws=ws_1, check=False)
+            d_ev[i][1].record()
+        torch.cuda.synchronize()
+        awq.check_workspace(ws_1, "w4a16 decode")
+        d_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in d_ev)[5], world)
+        d_bytes = Di * Do / 2 + 4.0 * T * Do + 2.0 * (Di + Do) + 4.0 * Di
+        w4["decode_m1"] = {"us": d_ms * 1e3, "bytes": d_bytes, "gbs": d_bytes / (d_ms * 1e-3) / 1e9,
+                           "frac_hbm": d_bytes / (d_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "bound": "hbm"}
 
     # ---- the adr's greedy search on the same layer (separate from the step)
     gr = None

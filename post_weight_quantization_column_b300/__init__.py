@@ -69,6 +69,7 @@ _SIGS = {
     "awq_greedy_workspace_size": ([_c_i64, _c_i64, ctypes.POINTER(awq_cfg), ctypes.POINTER(_c_sz)], ctypes.c_int),
     "awq_greedy_search": ([_vp, _vp, _c_i64, _c_i64, ctypes.POINTER(awq_cfg), _c_i32, _c_i32, _c_i32, _vp, _vp, _vp,
                            _vp, _c_sz, _vp], ctypes.c_int),
+    "awq_w4a16_workspace_size": ([_c_i64, _c_i64, _c_i64, ctypes.POINTER(_c_sz)], ctypes.c_int),
     "awq_w4a16_matmul": ([_vp, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp, ctypes.POINTER(awq_cfg), _vp, _vp, _c_sz,
                           _vp], ctypes.c_int),
     "awq_selftest_gemm_bf16": ([_vp, _vp, _c_i32, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_sz, _vp], ctypes.c_int),
@@ -363,6 +364,12 @@ def greedy_search(W: torch.Tensor, mean_abs: torch.Tensor, group_size: int = 128
 
 
 # ---------------------------------------------------------------------- after the path
+def w4a16_workspace_size(M: int, D_in: int, D_out: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().awq_w4a16_workspace_size(M, D_in, D_out, ctypes.byref(n)), "awq_w4a16_workspace_size")
+    return max(n.value, 256)
+
+
 def w4a16_matmul(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
                  s: Optional[torch.Tensor] = None, group_size: int = 128, out: Optional[torch.Tensor] = None,
                  ws: Optional[torch.Tensor] = None, stream=None, check: bool = True) -> torch.Tensor:
@@ -380,7 +387,7 @@ def w4a16_matmul(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, z
     if out is None:
         out = torch.empty(M, D_out, dtype=torch.bfloat16, device=X.device)
     if ws is None:
-        ws = _alloc_ws(256, X.device)
+        ws = _alloc_ws(w4a16_workspace_size(M, D_in, D_out), X.device)
     cfg = make_cfg(group_size)
     _check(lib().awq_w4a16_matmul(_ptr(X), M, D_in, D_out, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(s),
                                   ctypes.byref(cfg), _ptr(out), _ptr(ws), ws.numel(), _stream_handle(stream)),

@@ -534,6 +534,23 @@ awq_status awq_greedy_search(const void* W, const float* mean_abs, int64_t D_in,
 }
 
 // ------------------------------------------------------------------ W4A16 product
+namespace {
+// W4A16 workspace: header | (decode path) tickets [D_out/256] | partials [D_in/256][M][D_out]
+size_t w4a16_ticket_bytes(int64_t D_out) { return align_up(static_cast<size_t>(w4a16_decode_tickets(D_out)) * 4, 256); }
+size_t w4a16_ws_bytes(int64_t M, int64_t D_in, int64_t D_out) {
+  if (M > kW4a16DecodeMaxRows) return kHeaderBytes;
+  return kHeaderBytes + w4a16_ticket_bytes(D_out) +
+         align_up(static_cast<size_t>(w4a16_decode_partial_floats(M, D_in, D_out)) * 4, 256);
+}
+}  // namespace
+
+awq_status awq_w4a16_workspace_size(int64_t M, int64_t D_in, int64_t D_out, size_t* bytes) {
+  if (!bytes) return AWQ_ERR_INVALID_ARG;
+  if (M < 0 || D_in < 0 || D_out < 0) return AWQ_ERR_SHAPE;
+  *bytes = w4a16_ws_bytes(M, D_in, D_out);
+  return AWQ_OK;
+}
+
 awq_status awq_w4a16_matmul(const void* X, int64_t M, int64_t D_in, int64_t D_out, const uint8_t* qweight,
                             const void* scales, const void* zeros, const float* s, const awq_cfg* cfg, void* Y,
                             void* ws, size_t ws_bytes, awq_stream_t stream) {
@@ -547,10 +564,21 @@ awq_status awq_w4a16_matmul(const void* X, int64_t M, int64_t D_in, int64_t D_ou
   if (!aligned(X, 16) || !aligned(qweight, 16) || !aligned(scales, 16) || !aligned(zeros, 16) ||
       (s && !aligned(s, 16)) || !aligned(Y, 16) || !aligned(ws, 256))
     return AWQ_ERR_ALIGNMENT;
-  if (ws_bytes < kHeaderBytes) return AWQ_ERR_WORKSPACE;
+  if (ws_bytes < w4a16_ws_bytes(M, D_in, D_out)) return AWQ_ERR_WORKSPACE;
   int dev = 0;
   st = check_device(&dev);
   if (st != AWQ_OK) return st;
+  if (M <= kW4a16DecodeMaxRows) {
+    // a few rows: the CUDA-core path that reads the codes once
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const size_t tb = w4a16_ticket_bytes(D_out);
+    if (cudaMemsetAsync(ws, 0, kHeaderBytes + tb, cs) != cudaSuccess) return AWQ_ERR_CUDA;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    ProfScope prof("w4a16_decode", cs);
+    return from_cuda(launch_w4a16_decode(X, M, D_in, D_out, qweight, scales, zeros, s, cfg->group_size, Y,
+                                         reinterpret_cast<float*>(base + kHeaderBytes + tb),
+                                         reinterpret_cast<unsigned int*>(base + kHeaderBytes), cs));
+  }
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   st = get_encode(&encode);
   if (st != AWQ_OK) return st;

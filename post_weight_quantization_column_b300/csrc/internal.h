@@ -85,6 +85,13 @@ cudaError_t launch_gemm_store(PFN_cuTensorMapEncodeTiled_v12000 encode, const vo
 int search_fused_m_tiles(int64_t N);
 // CTA pairs that fit on the device at once (occupancy query).
 cudaError_t search_fused_max_pairs(int* pairs);
+// Decode-sized W4A16 product (M <= kW4a16DecodeMaxRows) on CUDA cores.
+constexpr int64_t kW4a16DecodeMaxRows = 4;
+int64_t w4a16_decode_partial_floats(int64_t M, int64_t D_in, int64_t D_out);
+int64_t w4a16_decode_tickets(int64_t D_out);
+cudaError_t launch_w4a16_decode(const void* X, int64_t M, int64_t D_in, int64_t D_out, const uint8_t* qweight,
+                                const void* scales, const void* zeros, const float* s, int group_size, void* Y,
+                                float* partial, unsigned int* tickets, cudaStream_t stream);
 // The adr's per-group coordinate greedy over power-of-two scales 2^k,
 // k = k_min .. k_min + ncand - 1 (ncand <= kMaxGreedyCand).
 constexpr int kMaxGreedyCand = 24;

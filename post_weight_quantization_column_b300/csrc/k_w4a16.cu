@@ -476,4 +476,192 @@ cudaError_t launch_w4a16(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X
   return cudaLaunchKernelEx(&cfg, w4a16_kernel, tmX, tmC, tmSc, tmZ, tmS, a);
 }
 
+// ---------------------------------------------------------------------------
+// Decode-sized W4A16 product (M <= 4 rows of X): the codes are read once and
+// the work is a handful of FMAs per weight, so CUDA cores keep up with HBM.
+// A CTA owns 256 columns x 256 input rows; warp w takes rows 32w .. 32w+31
+// (inside one group for every group size), lane l columns 8l .. 8l+7, one
+// 8-byte code load per byte row.  x' = x / s of the CTA's rows sits in shared
+// memory.  Per group the dequantisation is factored out of the sum:
+//   sum_j x'_j (q_j - z) sc = sc (sum_j x'_j q_j - z sum_j x'_j),
+// so a weight costs a nibble unpack and one FMA per row of X.  The 8 warps'
+// sums are added in warp order, the CTA's partial goes to the workspace, and
+// the last CTA of a column block (ticket) adds the row blocks in order (fp64)
+// and writes Y in bf16.
+namespace {
+
+constexpr int kDecCols = 256;       // columns per CTA (32 lanes x 8)
+constexpr int kDecRows = 256;       // input rows per CTA (8 warps x 32)
+constexpr int kDecThreads = 256;
+
+template <int MT>
+__global__ void __launch_bounds__(kDecThreads)
+    w4a16_decode_kernel(const __nv_bfloat16* __restrict__ X, int M, int64_t D_in, int64_t D_out,
+                        const uint8_t* __restrict__ qweight, const __half* __restrict__ scales,
+                        const __half* __restrict__ zeros, const float* __restrict__ s, int group_size,
+                        float* __restrict__ partial, unsigned int* __restrict__ tickets, __nv_bfloat16* __restrict__ Y) {
+  __shared__ float xs[MT][kDecRows];                  // x' = x / s of the CTA's rows
+  __shared__ float red[kDecThreads / 64][MT][kDecCols];  // warps w and w + 4 add into slot w
+  __shared__ bool last;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kDecCols;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kDecRows;
+  const int rows = static_cast<int>(min(static_cast<int64_t>(kDecRows), D_in - r0));  // a multiple of 64
+  for (int i = t; i < MT * kDecRows; i += kDecThreads) {
+    const int m = i / kDecRows, r = i % kDecRows;
+    float v = 0.f;
+    if (m < M && r < rows) {
+      v = __bfloat162float(X[static_cast<int64_t>(m) * D_in + r0 + r]);
+      if (s) v = __fdiv_rn(v, s[r0 + r]);
+    }
+    xs[m][r] = v;
+  }
+  __syncthreads();
+
+  const int64_t n = n0 + lane * 8;
+  float acc[MT][8];  // sum_j x'_j q_j of the warp's rows, then its share of Y
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[m][c] = 0.f;
+  const int wr = warp * 32;  // the warp's first row within the CTA
+  if (wr < rows && n < D_out) {
+    const uint8_t* qb = qweight + ((r0 + wr) / 2) * D_out + n;
+    // the warp's 16 byte rows in batches whose loads are all in flight: one
+    // batch of 16 for one or two rows of X, two of 8 when the accumulators
+    // need the registers
+    constexpr int kBatch = MT <= 2 ? 16 : 8;
+#pragma unroll
+    for (int h = 0; h < 16 / kBatch; ++h) {
+      uint2 cb[kBatch];
+#pragma unroll
+      for (int p = 0; p < kBatch; ++p) cb[p] = *reinterpret_cast<const uint2*>(qb + (kBatch * h + p) * D_out);
+#pragma unroll
+      for (int p = 0; p < kBatch; ++p) {
+#pragma unroll
+        for (int odd = 0; odd < 2; ++odd) {
+          float t0[4], t1[4];
+          nibbles_to_f32(odd ? (cb[p].x >> 4) & 0x0F0F0F0Fu : cb[p].x & 0x0F0F0F0Fu, t0);
+          nibbles_to_f32(odd ? (cb[p].y >> 4) & 0x0F0F0F0Fu : cb[p].y & 0x0F0F0F0Fu, t1);
+          float qc[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            qc[k] = t0[k] - 8388608.0f;  // the code, exact
+            qc[4 + k] = t1[k] - 8388608.0f;
+          }
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const float x = xs[m][wr + 2 * (kBatch * h + p) + odd];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[m][c] = fmaf(x, qc[c], acc[m][c]);
+          }
+        }
+      }
+    }
+    // the warp's rows lie in one group: scale and zero of its 8 columns
+    const int64_t g = (r0 + wr) / group_size;
+    const uint4 hs = *reinterpret_cast<const uint4*>(scales + g * D_out + n);
+    const uint4 hz = *reinterpret_cast<const uint4*>(zeros + g * D_out + n);
+    const uint32_t us[4] = {hs.x, hs.y, hs.z, hs.w};
+    const uint32_t uz[4] = {hz.x, hz.y, hz.z, hz.w};
+    float sc[8], zc[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&us[k]));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&uz[k]));
+      sc[2 * k] = a.x;
+      sc[2 * k + 1] = a.y;
+      zc[2 * k] = b.x;
+      zc[2 * k + 1] = b.y;
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float xsum = 0.f;
+#pragma unroll 8
+      for (int r = 0; r < 32; ++r) xsum += xs[m][wr + r];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[m][c] = sc[c] * fmaf(-zc[c], xsum, acc[m][c]);
+    }
+  }
+  // the 8 warps' shares in a fixed order: (w0 + w4) + (w1 + w5) + (w2 + w6) + (w3 + w7)
+  if (warp < 4) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float4* dst = reinterpret_cast<float4*>(&red[warp][m][lane * 8]);
+      dst[0] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+      dst[1] = make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
+    }
+  }
+  __syncthreads();
+  if (warp >= 4) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float4* dst = reinterpret_cast<float4*>(&red[warp - 4][m][lane * 8]);
+      const float4 a = dst[0], b = dst[1];
+      dst[0] = make_float4(a.x + acc[m][0], a.y + acc[m][1], a.z + acc[m][2], a.w + acc[m][3]);
+      dst[1] = make_float4(b.x + acc[m][4], b.y + acc[m][5], b.z + acc[m][6], b.w + acc[m][7]);
+    }
+  }
+  __syncthreads();
+  const int64_t rb_count = gridDim.y;
+  for (int i = t; i < MT * kDecCols; i += kDecThreads) {
+    const int m = i / kDecCols, c = i % kDecCols;
+    if (m < M && n0 + c < D_out) {
+      const float v = (red[0][m][c] + red[1][m][c]) + (red[2][m][c] + red[3][m][c]);
+      partial[(static_cast<int64_t>(blockIdx.y) * M + m) * D_out + n0 + c] = v;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (t == 0) last = atomicAdd(&tickets[blockIdx.x], 1u) == static_cast<unsigned>(rb_count) - 1u;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int i = t; i < MT * kDecCols; i += kDecThreads) {
+    const int m = i / kDecCols, c = i % kDecCols;
+    if (m < M && n0 + c < D_out) {
+      double v = 0.0;
+      for (int64_t b0 = 0; b0 < rb_count; b0 += 16) {
+        float pv[16];  // 16 row blocks' loads in flight, added in block order
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          pv[k] = b0 + k < rb_count ? partial[((b0 + k) * M + m) * D_out + n0 + c] : 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v += static_cast<double>(pv[k]);
+      }
+      Y[static_cast<int64_t>(m) * D_out + n0 + c] = __float2bfloat16_rn(static_cast<float>(v));
+    }
+  }
+  if (t == 0) tickets[blockIdx.x] = 0u;  // ready for the next call
+}
+
+}  // namespace
+
+int64_t w4a16_decode_partial_floats(int64_t M, int64_t D_in, int64_t D_out) {
+  return ((D_in + kDecRows - 1) / kDecRows) * M * D_out;
+}
+int64_t w4a16_decode_tickets(int64_t D_out) { return (D_out + kDecCols - 1) / kDecCols; }
+
+cudaError_t launch_w4a16_decode(const void* X, int64_t M, int64_t D_in, int64_t D_out, const uint8_t* qweight,
+                                const void* scales, const void* zeros, const float* s, int group_size, void* Y,
+                                float* partial, unsigned int* tickets, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>((D_out + kDecCols - 1) / kDecCols),
+                  static_cast<unsigned>((D_in + kDecRows - 1) / kDecRows));
+  const auto* Xb = static_cast<const __nv_bfloat16*>(X);
+  const auto* sc = static_cast<const __half*>(scales);
+  const auto* zr = static_cast<const __half*>(zeros);
+  auto* Yb = static_cast<__nv_bfloat16*>(Y);
+  const int m = static_cast<int>(M);
+  if (M <= 1)
+    w4a16_decode_kernel<1><<<grid, kDecThreads, 0, stream>>>(Xb, m, D_in, D_out, qweight, sc, zr, s, group_size,
+                                                             partial, tickets, Yb);
+  else if (M <= 2)
+    w4a16_decode_kernel<2><<<grid, kDecThreads, 0, stream>>>(Xb, m, D_in, D_out, qweight, sc, zr, s, group_size,
+                                                             partial, tickets, Yb);
+  else
+    w4a16_decode_kernel<4><<<grid, kDecThreads, 0, stream>>>(Xb, m, D_in, D_out, qweight, sc, zr, s, group_size,
+                                                             partial, tickets, Yb);
+  return cudaGetLastError();
+}
+
 }  // namespace awqdev

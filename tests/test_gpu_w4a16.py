@@ -69,8 +69,13 @@ def _layer(seed, M, D_in, D_out, g, sym, alpha=0.5, w_sigma=0.02):
 
 CASES = [
     # M, D_in, D_out, group, symmetric: ragged rows (not a multiple of 512), ragged
-    # columns (not a multiple of 256), several K steps per group, every group size
+    # columns (not a multiple of 256), several K steps per group, every group size;
+    # M <= 4 takes the decode path (row blocks of 256 with a ragged last block)
     (1, 256, 272, 128, False),
+    (2, 320, 784, 64, True),
+    (3, 768, 1040, 256, False),
+    (5, 1024, 528, 128, True),
+    (8, 576, 4096, 64, False),
     (200, 384, 784, 64, True),
     (600, 512, 1040, 128, False),
     (513, 768, 528, 256, True),
@@ -149,3 +154,25 @@ def test_w4a16_full_size_sampled(awq, name):
     check_close(Ys, ref, Xf[rows], s, oq, osc, oz, w.group_size)
     del Xd, Wd, Y
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_w4a16_decode_full_size_sampled(awq, M):
+    """The large MLP layer's weights with a decode-sized X; the oracle checks
+    512 sampled columns."""
+    w = synth.WORKLOADS["large_mlp"]
+    rng = np.random.default_rng(200 + M)
+    Wf = (rng.standard_normal((w.D_in, w.D_out)) * 0.01).astype(np.float32)
+    Xf = rng.standard_normal((M, w.D_in)).astype(np.float32)
+    s = rng.uniform(0.5, 4.0, w.D_in).astype(np.float32)
+    Wb, Xb = synth.to_bf16(Wf), synth.to_bf16(Xf)
+    Wf, Xf = synth.bf16_to_f32(Wb), synth.bf16_to_f32(Xb)
+    sd = torch.from_numpy(s).cuda()
+    qw, sc, z = awq.quantize_pack(Wb.cuda(), sd, w.group_size, w.symmetric)
+    Y = awq.w4a16_matmul(Xb.cuda(), qw, sc, z, sd, group_size=w.group_size)
+    cols = synth.sample_columns(w.D_out, 512, w.seed)
+    oq, osc, oz = orc.pack(Wf[:, cols], s, w.group_size, w.symmetric)
+    assert np.array_equal(qw[:, cols].cpu().numpy(), oq)
+    Ys = Y[:, cols].float().cpu().numpy().astype(np.float64)
+    ref = orc.w4a16_matmul(Xf, oq, osc, oz, s, group_size=w.group_size)
+    check_close(Ys, ref, Xf, s, oq, osc, oz, w.group_size)
