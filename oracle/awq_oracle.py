@@ -298,7 +298,7 @@ def greedy_search(W, mean_abs, group_size=128, symmetric=False, passes=3, candid
     indices, errors float64 [passes, D_in, len(candidates)] of every
     evaluated candidate).  `follow`, if given ([passes, D_in] candidate
     indices), replaces each decision by the given one (used to replay another
-    implementation's choices and judge each against these errors).
+    implementation's choices and weigh each against these errors).
     """
     W = np.asarray(W, dtype=F32)
     a = np.asarray(mean_abs, dtype=np.float64)
