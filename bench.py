@@ -490,6 +490,36 @@ def run_ours(args, world, rank, local):
         w4["decode_m1"] = {"us": d_ms * 1e3, "bytes": d_bytes, "gbs": d_bytes / (d_ms * 1e-3) / 1e9,
                            "frac_hbm": d_bytes / (d_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "bound": "hbm"}
 
+    # ---- the same search through the Gram factor of X, where N > D_in (separate from the step)
+    gram = None
+    if N > Di and Di % 64 == 0:
+        ws_g = torch.empty(awq.search_gram_workspace_size(N, Di, Do, G, g, sym), dtype=torch.uint8, device=dev)
+        res_g = awq.SearchResult(torch.empty(G, dtype=torch.float64, device=dev),
+                                 torch.empty(1, dtype=torch.int32, device=dev),
+                                 torch.empty(Di, dtype=torch.float32, device=dev), None, grid, ws_g)
+        awq.search(Xd, Wd, a_buf, grid, g, sym, ws=ws_g, out=res_g, gram=True)
+        awq.search(Xd, Wd, a_buf, grid, g, sym, ws=ws_q, out=res)
+        torch.cuda.synchronize()
+        tg, td = [], []
+        for i in range(3):
+            for lst, kw in ((tg, dict(ws=ws_g, out=res_g, gram=True)), (td, dict(ws=ws_q, out=res))):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                flush_l2()
+                e0.record()
+                awq.search(Xd, Wd, a_buf, grid, g, sym, check=False, **kw)
+                e1.record()
+                lst.append((e0, e1))
+        torch.cuda.synchronize()
+        awq.check_workspace(ws_g, "search gram")
+        g_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in tg)[1], world)
+        d_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in td)[1], world)
+        rel = (res_g.losses - res.losses).abs().div(res.losses).max().item()
+        gram = {"workload": f"search through R = chol(X^T X)^T, {Di} rows instead of {N}", "ms": g_ms,
+                "direct_ms": d_ms, "speedup": d_ms / g_ms, "max_rel_loss_diff_vs_direct": rel,
+                "same_alpha_star": int(res_g.best_idx.item()) == int(res.best_idx.item()),
+                "timing": "median of 3 after one warm-up, L2 flushed before each"}
+        del ws_g
+
     # ---- the adr's greedy search on the same layer (separate from the step)
     gr = None
     g_ev = []
@@ -529,6 +559,7 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "w4a16": w4,
         "adr_greedy": gr,
+        "gram_search": gram,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         Xf, Wf = synth.bf16_to_f32(X), synth.bf16_to_f32(W)

@@ -219,6 +219,32 @@ AWQ_API awq_status awq_quantize_pack(const void* W, const float* s, int64_t D_in
                              void* ws, size_t ws_bytes, awq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The same search through the Gram matrix of X (N >= D_in).
+ *
+ * Every candidate's loss is a quadratic form in H = X^T X:
+ *     L_k = ||X D_k||^2 = sum_n d_n^T H d_n,   D_k = S_k^-1 W'hat_k - W,
+ * so with the Cholesky factor H = L L^T the search can run on R = L^T
+ * (D_in rows) in place of X (N rows): 2 D_in^2 D_out flops per candidate
+ * instead of 2 N D_in D_out, after one 2 N D_in^2 product for H and
+ * D_in^3 / 3 for the factor.  Worth it when N is well above D_in.
+ *
+ * Arguments, outputs and conventions as for awq_search; ws of
+ * awq_search_gram_workspace_size() bytes, which begins with a search
+ * workspace, so awq_quantize_pack_searched(search_ws = ws) works after it.
+ * H is accumulated in fp32 from the bf16 X on the tensor cores, factored in
+ * fp32 (64 x 64 blocks) and R rounded to bf16, so the losses differ from
+ * awq_search's by the rounding of R (well inside the 1e-2 loss tolerance on
+ * the test layers).  A factor that is not positive definite (rank-deficient
+ * X) sets AWQ_ERR_RANGE.  Requires N >= D_in and D_in a multiple of 64.
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_search_gram_workspace_size(int64_t N, int64_t D_in, int64_t D_out, int32_t G,
+                                                  const awq_cfg* cfg, size_t* bytes);
+AWQ_API awq_status awq_search_gram(const void* X, const void* W, int64_t N, int64_t D_in, int64_t D_out,
+                                   const float* mean_abs, const double* grid, int32_t G, const awq_cfg* cfg,
+                                   double* losses, int32_t* best_idx, float* s_star, double* col_losses, void* ws,
+                                   size_t ws_bytes, awq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Step 4 right after a search: the same packing, with the per-group
  * quantiser parameters the search already computed for its best candidate.
  *

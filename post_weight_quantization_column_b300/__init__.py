@@ -59,6 +59,10 @@ _SIGS = {
                                    ctypes.POINTER(_c_sz)], ctypes.c_int),
     "awq_search": ([_vp, _vp, _c_i64, _c_i64, _c_i64, _vp, ctypes.POINTER(ctypes.c_double), _c_i32,
                     ctypes.POINTER(awq_cfg), _vp, _vp, _vp, _vp, _vp, _c_sz, _vp], ctypes.c_int),
+    "awq_search_gram_workspace_size": ([_c_i64, _c_i64, _c_i64, _c_i32, ctypes.POINTER(awq_cfg),
+                                        ctypes.POINTER(_c_sz)], ctypes.c_int),
+    "awq_search_gram": ([_vp, _vp, _c_i64, _c_i64, _c_i64, _vp, ctypes.POINTER(ctypes.c_double), _c_i32,
+                         ctypes.POINTER(awq_cfg), _vp, _vp, _vp, _vp, _vp, _c_sz, _vp], ctypes.c_int),
     "awq_pack_workspace_size": ([_c_i64, _c_i64, ctypes.POINTER(awq_cfg), ctypes.POINTER(_c_sz)], ctypes.c_int),
     "awq_quantize_pack": ([_vp, _vp, _c_i64, _c_i64, ctypes.POINTER(awq_cfg), _vp, _vp, _vp, _vp, _c_sz, _vp],
                           ctypes.c_int),
@@ -235,11 +239,21 @@ def search_workspace_size(N, D_in, D_out, G=21, group_size=128, symmetric=False,
     return n.value
 
 
+def search_gram_workspace_size(N, D_in, D_out, G=21, group_size=128, symmetric=False, act_floor=1e-4) -> int:
+    cfg = make_cfg(group_size, symmetric, 4, act_floor)
+    n = ctypes.c_size_t(0)
+    _check(lib().awq_search_gram_workspace_size(N, D_in, D_out, G, ctypes.byref(cfg), ctypes.byref(n)),
+           "awq_search_gram_workspace_size")
+    return n.value
+
+
 def search(X: torch.Tensor, W: torch.Tensor, mean_abs: torch.Tensor, grid=None, group_size: int = 128,
            symmetric: bool = False, act_floor: float = 1e-4, col_losses: bool = False,
            ws: Optional[torch.Tensor] = None, out: Optional[SearchResult] = None, stream=None,
-           check: bool = True) -> SearchResult:
-    """The alpha-grid scale search over X bf16 [N, D_in], W bf16 [D_in, D_out]."""
+           check: bool = True, gram: bool = False) -> SearchResult:
+    """The alpha-grid scale search over X bf16 [N, D_in], W bf16 [D_in, D_out].
+
+    gram=True evaluates the same losses through the Gram factor of X (N >= D_in): cheaper when N > D_in."""
     _need(X, torch.bfloat16, "X")
     _need(W, torch.bfloat16, "W")
     _need(mean_abs, torch.float32, "mean_abs")
@@ -252,7 +266,8 @@ def search(X: torch.Tensor, W: torch.Tensor, mean_abs: torch.Tensor, grid=None, 
     cfg = make_cfg(group_size, symmetric, 4, act_floor)
     dev = X.device
     if ws is None:
-        ws = _alloc_ws(search_workspace_size(N, D_in, D_out, G, group_size, symmetric, act_floor), dev)
+        size_fn = search_gram_workspace_size if gram else search_workspace_size
+        ws = _alloc_ws(size_fn(N, D_in, D_out, G, group_size, symmetric, act_floor), dev)
     if out is None:
         out = SearchResult(torch.empty(G, dtype=torch.float64, device=dev),
                            torch.empty(1, dtype=torch.int32, device=dev),
@@ -260,11 +275,13 @@ def search(X: torch.Tensor, W: torch.Tensor, mean_abs: torch.Tensor, grid=None, 
                            torch.empty(G, D_out, dtype=torch.float64, device=dev) if col_losses else None,
                            grid, ws)
     garr = (ctypes.c_double * G)(*grid)
-    _check(lib().awq_search(_ptr(X), _ptr(W), N, D_in, D_out, _ptr(mean_abs), garr, G, ctypes.byref(cfg),
-                            _ptr(out.losses), _ptr(out.best_idx), _ptr(out.s_star), _ptr(out.col_losses),
-                            _ptr(ws), ws.numel(), _stream_handle(stream)), "awq_search")
+    fn = lib().awq_search_gram if gram else lib().awq_search
+    name = "awq_search_gram" if gram else "awq_search"
+    _check(fn(_ptr(X), _ptr(W), N, D_in, D_out, _ptr(mean_abs), garr, G, ctypes.byref(cfg), _ptr(out.losses),
+              _ptr(out.best_idx), _ptr(out.s_star), _ptr(out.col_losses), _ptr(ws), ws.numel(),
+              _stream_handle(stream)), name)
     if check:
-        check_workspace(ws, "awq_search (device)", stream)
+        check_workspace(ws, f"{name} (device)", stream)
     return out
 
 

@@ -329,34 +329,17 @@ awq_status awq_search_workspace_size(int64_t N, int64_t D_in, int64_t D_out, int
   return AWQ_OK;
 }
 
-awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int64_t D_out, const float* mean_abs,
-                      const double* grid, int32_t G, const awq_cfg* cfg, double* losses, int32_t* best_idx,
-                      float* s_star, double* col_losses, void* ws, size_t ws_bytes, awq_stream_t stream) {
-  if (!X || !W || !mean_abs || !grid || !cfg || !losses || !best_idx || !s_star || !ws) return AWQ_ERR_INVALID_ARG;
-  awq_status st = validate_search_shape(N, D_in, D_out, G, cfg);
-  if (st != AWQ_OK) return st;
-  AlphaGrid ag;
-  std::memset(&ag, 0, sizeof(ag));
-  for (int k = 0; k < G; ++k) {
-    if (!std::isfinite(grid[k]) || grid[k] < 0.0 || grid[k] > 1.0) return AWQ_ERR_INVALID_ARG;
-    ag.a[k] = grid[k];
-  }
-  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(ws, 256) || !aligned(mean_abs, 4) || !aligned(s_star, 4) ||
-      !aligned(losses, 8) || !aligned(best_idx, 4) || (col_losses && !aligned(col_losses, 8)))
-    return AWQ_ERR_ALIGNMENT;
+namespace {
+// The search on "X" [N, D_in] (the calibration rows, or the Gram factor R
+// with N = D_in rows): scale table, group parameters, fused search, reduce.
+awq_status run_search(const void* X, const void* W, int64_t N, int64_t D_in, int64_t D_out, const float* mean_abs,
+                      const AlphaGrid& ag, int32_t G, const awq_cfg* cfg, double* losses, int32_t* best_idx,
+                      float* s_star, double* col_losses, void* ws, int dev, PFN_cuTensorMapEncodeTiled_v12000 encode,
+                      cudaStream_t s) {
   const SearchLayout L = search_layout(N, D_in, D_out, G, cfg->group_size);
-  if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
-  int dev = 0;
-  st = check_device(&dev);
-  if (st != AWQ_OK) return st;
-  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  st = get_encode(&encode);
-  if (st != AWQ_OK) return st;
   int pairs = 0;
-  st = get_pairs(dev, &pairs);
+  awq_status st = get_pairs(dev, &pairs);
   if (st != AWQ_OK) return st;
-
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
   uint32_t* status = status_word(ws);
   float* s_tab = reinterpret_cast<float*>(base + L.s_tab);
@@ -364,9 +347,6 @@ awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int
   float* qp = reinterpret_cast<float*>(base + L.qp);
   float* partial = reinterpret_cast<float*>(base + L.partial);
   double* col = col_losses ? col_losses : reinterpret_cast<double*>(base + L.col);
-
-  // status word and the reduction's ticket counter
-  if (cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return AWQ_ERR_CUDA;
   cudaError_t e;
   {
     ProfScope prof("scale_table", s);
@@ -388,6 +368,113 @@ awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int
                              s);
   }
   return from_cuda(e);
+}
+
+awq_status search_args(const void* X, const void* W, int64_t N, int64_t D_in, int64_t D_out, const float* mean_abs,
+                       const double* grid, int32_t G, const awq_cfg* cfg, double* losses, int32_t* best_idx,
+                       float* s_star, double* col_losses, void* ws, AlphaGrid* ag) {
+  if (!X || !W || !mean_abs || !grid || !cfg || !losses || !best_idx || !s_star || !ws) return AWQ_ERR_INVALID_ARG;
+  awq_status st = validate_search_shape(N, D_in, D_out, G, cfg);
+  if (st != AWQ_OK) return st;
+  std::memset(ag, 0, sizeof(*ag));
+  for (int k = 0; k < G; ++k) {
+    if (!std::isfinite(grid[k]) || grid[k] < 0.0 || grid[k] > 1.0) return AWQ_ERR_INVALID_ARG;
+    ag->a[k] = grid[k];
+  }
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(ws, 256) || !aligned(mean_abs, 4) || !aligned(s_star, 4) ||
+      !aligned(losses, 8) || !aligned(best_idx, 4) || (col_losses && !aligned(col_losses, 8)))
+    return AWQ_ERR_ALIGNMENT;
+  return AWQ_OK;
+}
+
+// Gram-form workspace: the search workspace for N = D_in rows (first, so that
+// the searched pack finds its group parameters at the usual offset) | H fp32
+// [D_in, D_in] | X^T bf16 [D_in, ldt], later R bf16 [D_in, D_in] in the same place
+struct GramLayout {
+  size_t h, t, total;
+  int64_t ldt;
+};
+GramLayout gram_layout(int64_t N, int64_t D_in, int64_t D_out, int G, int group_size) {
+  GramLayout L;
+  L.ldt = (N + kGemmBK - 1) / kGemmBK * kGemmBK;
+  L.h = align_up(search_layout(D_in, D_in, D_out, G, group_size).total, 256);
+  L.t = L.h + align_up(static_cast<size_t>(D_in) * static_cast<size_t>(D_in) * 4, 256);
+  const size_t tb = static_cast<size_t>(D_in) * static_cast<size_t>(L.ldt > D_in ? L.ldt : D_in) * 2;
+  L.total = L.t + align_up(tb, 256);
+  return L;
+}
+}  // namespace
+
+awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int64_t D_out, const float* mean_abs,
+                      const double* grid, int32_t G, const awq_cfg* cfg, double* losses, int32_t* best_idx,
+                      float* s_star, double* col_losses, void* ws, size_t ws_bytes, awq_stream_t stream) {
+  AlphaGrid ag;
+  awq_status st = search_args(X, W, N, D_in, D_out, mean_abs, grid, G, cfg, losses, best_idx, s_star, col_losses, ws,
+                              &ag);
+  if (st != AWQ_OK) return st;
+  if (ws_bytes < search_layout(N, D_in, D_out, G, cfg->group_size).total) return AWQ_ERR_WORKSPACE;
+  int dev = 0;
+  st = check_device(&dev);
+  if (st != AWQ_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  st = get_encode(&encode);
+  if (st != AWQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // status word and the reduction's ticket counter
+  if (cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return AWQ_ERR_CUDA;
+  return run_search(X, W, N, D_in, D_out, mean_abs, ag, G, cfg, losses, best_idx, s_star, col_losses, ws, dev,
+                    encode, s);
+}
+
+awq_status awq_search_gram_workspace_size(int64_t N, int64_t D_in, int64_t D_out, int32_t G, const awq_cfg* cfg,
+                                          size_t* bytes) {
+  if (!bytes) return AWQ_ERR_INVALID_ARG;
+  awq_status st = validate_search_shape(N, D_in, D_out, G, cfg);
+  if (st != AWQ_OK) return st;
+  if (N < D_in || D_in % 64 != 0) return AWQ_ERR_SHAPE;
+  *bytes = gram_layout(N, D_in, D_out, G, cfg->group_size).total;
+  return AWQ_OK;
+}
+
+awq_status awq_search_gram(const void* X, const void* W, int64_t N, int64_t D_in, int64_t D_out,
+                           const float* mean_abs, const double* grid, int32_t G, const awq_cfg* cfg, double* losses,
+                           int32_t* best_idx, float* s_star, double* col_losses, void* ws, size_t ws_bytes,
+                           awq_stream_t stream) {
+  AlphaGrid ag;
+  awq_status st = search_args(X, W, N, D_in, D_out, mean_abs, grid, G, cfg, losses, best_idx, s_star, col_losses, ws,
+                              &ag);
+  if (st != AWQ_OK) return st;
+  if (N < D_in || D_in % 64 != 0) return AWQ_ERR_SHAPE;
+  if (D_in > 65535 * static_cast<int64_t>(kGemmBM)) return AWQ_ERR_SHAPE;
+  const GramLayout G2 = gram_layout(N, D_in, D_out, G, cfg->group_size);
+  if (ws_bytes < G2.total) return AWQ_ERR_WORKSPACE;
+  int dev = 0;
+  st = check_device(&dev);
+  if (st != AWQ_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  st = get_encode(&encode);
+  if (st != AWQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* H = reinterpret_cast<float*>(base + G2.h);
+  void* T = base + G2.t;
+  if (cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return AWQ_ERR_CUDA;
+  cudaError_t e;
+  {
+    // H = X^T X from the zero-padded transpose (both operands K-major)
+    ProfScope prof("gram", s);
+    e = launch_transpose_x(X, N, D_in, G2.ldt, T, s);
+    if (e == cudaSuccess)
+      e = launch_gemm_store(encode, T, T, 0, D_in, D_in, G2.ldt, H, status_word(ws), s);
+  }
+  if (e == cudaSuccess) {
+    ProfScope prof("cholesky", s);
+    e = launch_cholesky(H, D_in, status_word(ws), s);
+    if (e == cudaSuccess) e = launch_lt_to_bf16(H, D_in, T, s);  // R = L^T over the dead transpose
+  }
+  if (e != cudaSuccess) return from_cuda(e);
+  return run_search(T, W, D_in, D_in, D_out, mean_abs, ag, G, cfg, losses, best_idx, s_star, col_losses, ws, dev,
+                    encode, s);
 }
 
 // ------------------------------------------------------------------ pack

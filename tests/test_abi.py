@@ -122,6 +122,10 @@ def test_calls_validate_before_cuda(L):
     assert L.awq_act_stats_accumulate(fake, 8, 256, 256, None, None, fake, 1 << 20, None) == 1
     assert L.awq_act_stats_accumulate(fake, 8, 256, 256, ctypes.c_void_p(0x1004), None, fake, 1 << 20, None) == 3
     assert L.awq_act_stats_finalize(fake, 0, 256, fake, None) == 2
+    # Gram-form search: fewer rows than channels
+    n = ctypes.c_size_t(0)
+    assert L.awq_search_gram_workspace_size(128, 256, 256, 21, ctypes.byref(cfg), ctypes.byref(n)) == 2
+    assert L.awq_search_gram_workspace_size(512, 256, 256, 21, ctypes.byref(cfg), ctypes.byref(n)) == 0 and n.value > 0
     # closed-form scale: alpha outside [0, 1], ragged D_out
     assert L.awq_closed_form_scales(fake, 256, 256, fake, 1.5, ctypes.byref(cfg), fake, None) == 1
     assert L.awq_closed_form_scales(fake, 256, 252, fake, 0.5, ctypes.byref(cfg), fake, None) == 2
