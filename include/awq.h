@@ -12,15 +12,26 @@
  *   3. awq_quantize_pack  Quantize(diag(s) W) as nibble-packed codes plus
  *                         fp16 per-group scales and zeros
  *
+ * and around them: the statistic over a stream of batches and its max form
+ * (awq_act_stats_accumulate / _finalize), the pack that reuses the search's
+ * quantiser parameters (awq_quantize_pack_searched), the same search through
+ * the Gram factor of X (awq_search_gram), the closed-form scale
+ * (awq_closed_form_scales), the ADR's per-group greedy search
+ * (awq_greedy_search), and the W4A16 product on the packed layer
+ * (awq_w4a16_matmul).
+ *
  * Sources, by page title and section:
  *   "AWQ (Activation-aware Weight Quantization)" (compassingai concept page):
  *       技术原理 - 重要通道识别的统计依据 (statistic), 缩放因子优化的完整流程
  *       steps 1-6 (grid, scaling, group quantisation, loss, argmin, s*),
  *       推理时的等效实现 (offline Quantize(diag(s*) W)), 量化数学基础 (absmax).
- *   aiqz.cc article "awq-activation-aware-quantization", sections 1 and 4
- *       (E|X_i| importance; Delta = max|w_s|/7, round, clamp, dequant).
- *   "009. AWQ Integration" (ADR), 关键设计 3 and Consequences (search and
- *       pack share one quantiser; two 4-bit weights per byte; zeros buffer).
+ *   aiqz.cc article "awq-activation-aware-quantization", sections 1, 3 and 4
+ *       (E|X_i| importance; the closed-form scale; Delta = max|w_s|/7, round,
+ *       clamp, dequant).
+ *   "009. AWQ Integration" (ADR), Decision, 关键设计 1-3 and Consequences
+ *       (add_batch statistic; per-group power-of-two greedy; search and pack
+ *       share one quantiser; two 4-bit weights per byte; zeros buffer).
+ *   "量化推理算法 GPTQ / AWQ" (slowleelab), L3 (H = X^T X).
  *   CSDN AutoAWQ deployment walkthrough, section 2 (quant_config:
  *       zero_point, q_group_size 128, w_bit 4).
  *
