@@ -389,16 +389,18 @@ awq_status search_args(const void* X, const void* W, int64_t N, int64_t D_in, in
 
 // Gram-form workspace: the search workspace for N = D_in rows (first, so that
 // the searched pack finds its group parameters at the usual offset) | H fp32
-// [D_in, D_in] | X^T bf16 [D_in, ldt], later R bf16 [D_in, D_in] in the same place
+// [D_in, D_in] | the inverse of one 64 x 64 Cholesky block (16 KB) | X^T bf16
+// [D_in, ldt], later R bf16 [D_in, D_in] in the same place
 struct GramLayout {
-  size_t h, t, total;
+  size_t h, linv, t, total;
   int64_t ldt;
 };
 GramLayout gram_layout(int64_t N, int64_t D_in, int64_t D_out, int G, int group_size) {
   GramLayout L;
   L.ldt = (N + kGemmBK - 1) / kGemmBK * kGemmBK;
   L.h = align_up(search_layout(D_in, D_in, D_out, G, group_size).total, 256);
-  L.t = L.h + align_up(static_cast<size_t>(D_in) * static_cast<size_t>(D_in) * 4, 256);
+  L.linv = L.h + align_up(static_cast<size_t>(D_in) * static_cast<size_t>(D_in) * 4, 256);
+  L.t = L.linv + 64 * 64 * 4;
   const size_t tb = static_cast<size_t>(D_in) * static_cast<size_t>(L.ldt > D_in ? L.ldt : D_in) * 2;
   L.total = L.t + align_up(tb, 256);
   return L;
@@ -469,7 +471,7 @@ awq_status awq_search_gram(const void* X, const void* W, int64_t N, int64_t D_in
   }
   if (e == cudaSuccess) {
     ProfScope prof("cholesky", s);
-    e = launch_cholesky(H, D_in, status_word(ws), s);
+    e = launch_cholesky(H, D_in, reinterpret_cast<float*>(base + G2.linv), status_word(ws), s);
     if (e == cudaSuccess) e = launch_lt_to_bf16(H, D_in, T, s);  // R = L^T over the dead transpose
   }
   if (e != cudaSuccess) return from_cuda(e);

@@ -93,9 +93,10 @@ cudaError_t launch_w4a16_decode(const void* X, int64_t M, int64_t D_in, int64_t 
                                 const void* scales, const void* zeros, const float* s, int group_size, void* Y,
                                 float* partial, unsigned int* tickets, cudaStream_t stream);
 // The Gram form of the search: X^T (zero past N, row length ldt), the
-// blocked fp32 Cholesky of H in place (lower), R = L^T in bf16.
+// blocked fp32 Cholesky of H in place (lower; Linv: a 64 x 64 fp32 scratch
+// block), R = L^T in bf16.
 cudaError_t launch_transpose_x(const void* X, int64_t N, int64_t D, int64_t ldt, void* Xt, cudaStream_t stream);
-cudaError_t launch_cholesky(float* A, int64_t D, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_cholesky(float* A, int64_t D, float* Linv, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_lt_to_bf16(const float* L, int64_t D, void* R, cudaStream_t stream);
 // The adr's per-group coordinate greedy over power-of-two scales 2^k,
 // k = k_min .. k_min + ncand - 1 (ncand <= kMaxGreedyCand).

@@ -5,9 +5,10 @@
 // the same losses with D_in / N of the flops.  This file holds the steps that
 // build R: a tiled transpose of X (so that the tensor-core GEMM can form
 // X^T X from a K-major operand), a right-looking blocked Cholesky in fp32
-// (64 x 64 blocks: the diagonal block factored in shared memory, the panel
-// below it by forward substitution, the trailing lower triangle updated by a
-// register-tiled product), and the transposed conversion of L to bf16 R.
+// (64 x 64 blocks: the diagonal block factored in shared memory together
+// with its triangular inverse, the panel below it as a product with that
+// inverse, the trailing lower triangle updated by a register-tiled product),
+// and the transposed conversion of L to bf16 R.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -36,66 +37,103 @@ __global__ void transpose_x_kernel(const __nv_bfloat16* __restrict__ X, int64_t 
   }
 }
 
-// Factor the diagonal block (k, k) in place: A_kk = L_kk L_kk^T.
-__global__ void chol_diag_kernel(float* __restrict__ A, int64_t D, int k, uint32_t* status) {
+// Factor the diagonal block (k, k) in place, A_kk = L_kk L_kk^T, and write
+// the inverse of L_kk (lower triangular, zeros above) to Linv.  Per column j
+// of the block: every thread reads the pivot, the column below it is scaled
+// (barrier), the trailing lower triangle is updated by a 16 x 16 thread grid
+// (barrier).  The diagonal of L goes to a separate array so that the pivot
+// the threads read is never overwritten inside a step.  The inverse is
+// formed by one thread per column (forward substitution on the identity).
+__global__ void __launch_bounds__(256) chol_diag_kernel(float* __restrict__ A, int64_t D, int k,
+                                                        float* __restrict__ Linv, uint32_t* status) {
   __shared__ float S[kCb][kCb + 1];
-  const int t = threadIdx.x;  // 256
+  __shared__ float Li[kCb][kCb + 1];
+  __shared__ float Ld[kCb];
+  const int t = threadIdx.x;
+  const int ty = t / 16, tx = t % 16;
   const int64_t o = static_cast<int64_t>(k) * kCb;
-  for (int i = t; i < kCb * kCb; i += blockDim.x) S[i / kCb][i % kCb] = A[(o + i / kCb) * D + o + i % kCb];
+  for (int i = t; i < kCb * kCb; i += 256) S[i / kCb][i % kCb] = A[(o + i / kCb) * D + o + i % kCb];
   __syncthreads();
   for (int j = 0; j < kCb; ++j) {
-    if (t == 0) {
-      float d = S[j][j];
-      if (!(d > 0.f) || !isfinite(d)) {
-        set_error(status, AWQ_DEV_RANGE);  // not positive definite
-        d = 1.f;
-      }
-      S[j][j] = __fsqrt_rn(d);
+    float d = S[j][j];
+    if (!(d > 0.f) || !isfinite(d)) {
+      if (t == 0) set_error(status, AWQ_DEV_RANGE);  // not positive definite
+      d = 1.f;
     }
+    const float ljj = __fsqrt_rn(d);
+    if (t == 0) Ld[j] = ljj;
+    if (t > j && t < kCb) S[t][j] = __fdiv_rn(S[t][j], ljj);
     __syncthreads();
-    for (int i = j + 1 + t; i < kCb; i += blockDim.x) S[i][j] = __fdiv_rn(S[i][j], S[j][j]);
-    __syncthreads();
-    const int n = kCb - j - 1;  // trailing rows / columns
-    for (int e = t; e < n * n; e += blockDim.x) {
-      const int i = j + 1 + e / n, c = j + 1 + e % n;
-      if (c <= i) S[i][c] = fmaf(-S[i][j], S[c][j], S[i][c]);
+    for (int i = j + 1 + ty; i < kCb; i += 16) {
+      const float sij = S[i][j];
+      for (int c = j + 1 + tx; c <= i; c += 16) S[i][c] = fmaf(-sij, S[c][j], S[i][c]);
     }
     __syncthreads();
   }
-  for (int i = t; i < kCb * kCb; i += blockDim.x) {
+  for (int i = t; i < kCb * kCb; i += 256) {
     const int r = i / kCb, c = i % kCb;
-    if (c <= r) A[(o + r) * D + o + c] = S[r][c];
+    if (c < r) A[(o + r) * D + o + c] = S[r][c];
+    if (c == r) A[(o + r) * D + o + c] = Ld[r];
   }
+  if (t < kCb) {
+    const int m = t;  // column m of L^-1: rows m .. 63
+    for (int r = 0; r < kCb; ++r) {
+      float v = r == m ? 1.f : 0.f;
+      if (r > m)
+        for (int c = m; c < r; ++c) v = fmaf(-S[r][c], Li[c][m], v);
+      Li[r][m] = r < m ? 0.f : __fdiv_rn(v, Ld[r]);
+    }
+  }
+  __syncthreads();
+  for (int i = t; i < kCb * kCb; i += 256) Linv[i] = Li[i / kCb][i % kCb];
 }
 
-// Panel below block k: row i solves x L_kk^T = A[i, block k] by forward substitution.
-__global__ void chol_panel_kernel(float* __restrict__ A, int64_t D, int k) {
-  __shared__ float Lk[kCb][kCb + 1];
-  const int t = threadIdx.x;  // 128
+// Panel below block k: X L_kk^T = A[rows, block k], i.e. X = A L_kk^-T:
+// X[r][j] = sum_{c <= j} A[r][c] Linv[j][c], 64 rows x 64 columns per CTA,
+// 4 x 4 outputs per thread, read from shared memory before any is written.
+__global__ void __launch_bounds__(256) chol_panel_kernel(float* __restrict__ A, int64_t D, int k,
+                                                         const float* __restrict__ Linv) {
+  __shared__ float P[kCb][kCb + 1];
+  __shared__ float Li[kCb][kCb + 1];
+  const int t = threadIdx.x;
   const int64_t o = static_cast<int64_t>(k) * kCb;
-  for (int i = t; i < kCb * kCb; i += blockDim.x) Lk[i / kCb][i % kCb] = A[(o + i / kCb) * D + o + i % kCb];
+  const int64_t r0 = o + kCb + static_cast<int64_t>(blockIdx.x) * kCb;
+  for (int e = t; e < kCb * kCb / 4; e += 256) {
+    const int r = e / (kCb / 4), c4 = (e % (kCb / 4)) * 4;
+    const float4 v = *reinterpret_cast<const float4*>(A + (r0 + r) * D + o + c4);
+    const float4 w = *reinterpret_cast<const float4*>(Linv + r * kCb + c4);
+    P[r][c4] = v.x;
+    P[r][c4 + 1] = v.y;
+    P[r][c4 + 2] = v.z;
+    P[r][c4 + 3] = v.w;
+    Li[r][c4] = w.x;
+    Li[r][c4 + 1] = w.y;
+    Li[r][c4 + 2] = w.z;
+    Li[r][c4 + 3] = w.w;
+  }
   __syncthreads();
-  const int64_t row = o + kCb + static_cast<int64_t>(blockIdx.x) * blockDim.x + t;
-  if (row >= D) return;
-  float* a = A + row * D + o;
-  float x[kCb];
+  const int ty = t / 16, tx = t % 16;  // rows 4 ty .. 4 ty + 3, columns tx + 16 b
+  float acc[4][4];
 #pragma unroll
-  for (int c = 0; c < kCb; c += 4) {
-    const float4 v = *reinterpret_cast<const float4*>(a + c);
-    x[c] = v.x;
-    x[c + 1] = v.y;
-    x[c + 2] = v.z;
-    x[c + 3] = v.w;
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 8
+  for (int c = 0; c < kCb; ++c) {
+    float pr[4], lj[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) pr[a] = P[4 * ty + a][c];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) lj[b] = Li[tx + 16 * b][c];  // zero for c > j
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(pr[a], lj[b], acc[a][b]);
   }
 #pragma unroll
-  for (int j = 0; j < kCb; ++j) {
-    float v = x[j];
+  for (int a = 0; a < 4; ++a)
 #pragma unroll
-    for (int c = 0; c < j; ++c) v = fmaf(-x[c], Lk[j][c], v);
-    x[j] = __fdiv_rn(v, Lk[j][j]);
-  }
-#pragma unroll
-  for (int c = 0; c < kCb; c += 4) *reinterpret_cast<float4*>(a + c) = make_float4(x[c], x[c + 1], x[c + 2], x[c + 3]);
+    for (int b = 0; b < 4; ++b) A[(r0 + 4 * ty + a) * D + o + tx + 16 * b] = acc[a][b];
 }
 
 // Trailing update after block k: A[I, J] -= P_I P_J^T for the lower block
@@ -181,14 +219,13 @@ cudaError_t launch_transpose_x(const void* X, int64_t N, int64_t D, int64_t ldt,
   return cudaGetLastError();
 }
 
-cudaError_t launch_cholesky(float* A, int64_t D, uint32_t* status, cudaStream_t stream) {
+cudaError_t launch_cholesky(float* A, int64_t D, float* Linv, uint32_t* status, cudaStream_t stream) {
   const int nb = static_cast<int>(D / kCb);
   for (int k = 0; k < nb; ++k) {
-    chol_diag_kernel<<<1, 256, 0, stream>>>(A, D, k, status);
+    chol_diag_kernel<<<1, 256, 0, stream>>>(A, D, k, Linv, status);
     const int rest = nb - k - 1;  // trailing block rows
     if (rest > 0) {
-      const int64_t rows = static_cast<int64_t>(rest) * kCb;
-      chol_panel_kernel<<<static_cast<unsigned>((rows + 127) / 128), 128, 0, stream>>>(A, D, k);
+      chol_panel_kernel<<<static_cast<unsigned>(rest), 256, 0, stream>>>(A, D, k, Linv);
       const int64_t tiles = static_cast<int64_t>(rest) * (rest + 1) / 2;
       chol_update_kernel<<<static_cast<unsigned>(tiles), 256, 0, stream>>>(A, D, k);
     }
