@@ -448,6 +448,29 @@ def run_ours(args, world, rank, local):
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
     e2e_ms = max_over_ranks(e2e_ms, world)
 
+    # ---- awq_quantize_pack at the step's s* on its own: the pack for any s,
+    # which also forms the group ranges (separate from the step)
+    pk2 = tuple(torch.empty_like(t) for t in pk)
+    ws_p = torch.empty(256, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        awq.quantize_pack(Wd, res.s_star, g, sym, out=pk2, ws=ws_p, check=False)
+    p_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+    for i in range(10):
+        flush_l2()
+        p_ev[i][0].record()
+        awq.quantize_pack(Wd, res.s_star, g, sym, out=pk2, ws=ws_p, check=False)
+        p_ev[i][1].record()
+    torch.cuda.synchronize()
+    awq.check_workspace(ws_p, "pack")
+    same = all(torch.equal(a, b) for a, b in zip(pk, pk2))
+    p_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in p_ev)[5], world)
+    p_bytes = 2.0 * Di * Do + 4.0 * Di + Di * Do / 2.0 + 4.0 * Do * Di / g
+    pack_any = {"workload": f"awq_quantize_pack(W, s*), D_in={Di} D_out={Do} g={g}", "us": p_ms * 1e3,
+                "bytes": p_bytes, "gbs": p_bytes / (p_ms * 1e-3) / 1e9,
+                "frac_hbm": p_bytes / (p_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "bound": "hbm",
+                "equals_searched_pack": same, "timing": "median of 10 launches, L2 flushed before each"}
+    del pk2
+
     # ---- after the path: the W4A16 product of the step's packed layer on its
     # own activations, Y = (X diag(1/s*)) Dequant(qweight); separate from the step
     w4 = None
@@ -560,6 +583,7 @@ def run_ours(args, world, rank, local):
         "w4a16": w4,
         "adr_greedy": gr,
         "gram_search": gram,
+        "pack_any_s": pack_any,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         Xf, Wf = synth.bf16_to_f32(X), synth.bf16_to_f32(W)

@@ -506,17 +506,11 @@ awq_status awq_quantize_pack(const void* W, const float* s, int64_t D_in, int64_
   int dev = 0;
   st = check_device(&dev);
   if (st != AWQ_OK) return st;
-  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  st = get_encode(&encode);
-  if (st != AWQ_OK) return st;
-  int sms = 0;
-  st = get_sms(dev, &sms);
-  if (st != AWQ_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return AWQ_ERR_CUDA;
   ProfScope prof("pack", cs);
-  return from_cuda(launch_pack(encode, W, s, D_in, D_out, cfg->group_size, cfg->symmetric, qweight, scales, zeros,
-                               status_word(ws), sms, cs));
+  return from_cuda(launch_pack(W, s, D_in, D_out, cfg->group_size, cfg->symmetric, qweight, scales, zeros,
+                               status_word(ws), cs));
 }
 
 awq_status awq_quantize_pack_searched(const void* W, int64_t D_in, int64_t D_out, int32_t G, const awq_cfg* cfg,

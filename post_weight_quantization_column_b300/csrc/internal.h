@@ -61,9 +61,8 @@ cudaError_t launch_closed_form(const void* W, int64_t D_in, int64_t D_out, const
                                float act_floor, float* s_out, cudaStream_t stream);
 cudaError_t launch_group_params(const void* W, const float* s_tab, int64_t D_in, int64_t D_out, int G,
                                 int group_size, int symmetric, float* qp, uint32_t* status, cudaStream_t stream);
-cudaError_t launch_pack(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* W, const float* s, int64_t D_in,
-                        int64_t D_out, int group_size, int symmetric, uint8_t* qweight, void* scales, void* zeros,
-                        uint32_t* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_pack(const void* W, const float* s, int64_t D_in, int64_t D_out, int group_size, int symmetric,
+                        uint8_t* qweight, void* scales, void* zeros, uint32_t* status, cudaStream_t stream);
 // Pack with the group parameters a search computed for its best candidate
 // (qp: the search workspace's parameter table, best_idx: device int32).
 cudaError_t launch_pack_searched(const void* W, const float* s, const float* qp, const int32_t* best_idx, int G,
