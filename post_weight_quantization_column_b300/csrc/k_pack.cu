@@ -85,9 +85,12 @@ __device__ __forceinline__ float maxabs3(float a, float b, float c) {
 // integer code; d = rint - w'/step (one more fma) is within 1/2 of it, and
 // the returned maximum |d| flags a near tie anywhere in the thread's
 // elements.  Each packed byte is c_even + 16 c_odd in the low bits
-// (1.5*2^23 has a zero low byte).  Asymmetric codes cannot fall below 0 on
-// this path: rint is odd, so the group minimum gets rint(min/step) +
-// rint(-min/step) = 0 and every other element more.
+// (1.5*2^23 has a zero low byte).  Asymmetric codes get no lower clamp here:
+// rint is odd, so while the zero equals rint(-min/step) the group minimum
+// gets code 0 and every other element more.  That fails only where the zero
+// was clamped to 15 (a subnormal fp16 step that rounded far down can put
+// -min/step above 15.5), so callers send every thread with a zero of 15 in
+// its columns to the exact path (see has_zero15).
 // inv, zmz: 1/step and 1.5*2^23 + the stored offset (the zero; 8 for
 // symmetric codes) of the 8 columns; out[p]: the 8 bytes of row pair p.
 template <bool SYM>
@@ -174,6 +177,17 @@ __device__ __noinline__ void pack_exact_8x8(const __nv_bfloat16* __restrict__ W,
         make_uint2(bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24),
                    bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24));
   }
+}
+
+// An asymmetric zero of 15 in any of the thread's columns: the codes need
+// the lower clamp of the exact path (rare: one-signed negative groups).
+template <bool SYM>
+__device__ __forceinline__ bool has_zero15(const float (&zmz)[8]) {
+  if (SYM) return false;
+  bool z15 = false;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) z15 |= zmz[k] == kMagic + 15.f;
+  return z15;
 }
 
 __device__ __forceinline__ void store_codes_8x8(const uint32_t (&out)[kPackRows / 2][2], int64_t row0, int64_t n,
@@ -331,7 +345,7 @@ __global__ void __launch_bounds__(kPackThreads, 3)
     }
   }
   uint32_t out[kPackRows / 2][2];
-  if (codes_8x8<SYM>(w, sj, inv, zmz, out) > kTieGuard) {
+  if (codes_8x8<SYM>(w, sj, inv, zmz, out) > kTieGuard || has_zero15<SYM>(zmz)) {
     pack_exact_8x8<SYM>(W, s, qc, row0, n, D_out, qweight);
     return;
   }
@@ -426,7 +440,7 @@ __global__ void __launch_bounds__(kPackThreads, 3)
     *reinterpret_cast<uint4*>(zeros + g * D_out + n) = make_uint4(zr[0], zr[1], zr[2], zr[3]);
   }
   uint32_t out[kPackRows / 2][2];
-  if (codes_8x8<SYM>(w, sj, inv, zmz, out) > kTieGuard) {
+  if (codes_8x8<SYM>(w, sj, inv, zmz, out) > kTieGuard || has_zero15<SYM>(zmz)) {
     pack_exact_8x8<SYM>(W, s, qc, row0, n, D_out, qweight);
     return;
   }

@@ -171,3 +171,45 @@ def test_pack_searched_degenerate_groups_and_ties(awq):
         assert np.array_equal(qw.cpu().numpy(), oq)
         assert np.array_equal(sc.cpu().numpy().view(np.uint16), osc.view(np.uint16))
         assert np.array_equal(z.cpu().numpy().view(np.uint16), oz.view(np.uint16))
+
+
+def _subnormal_step_groups(rng, D_out, sym):
+    """Two groups of 128 rows: the first with so small a range that the fp16
+    step is subnormal and rounds far down (raw step 1.4 * 2^-24 -> 2^-24), the
+    second ordinary.  Asymmetric: the first group is negative, so -min/step =
+    21 and the zero is clamped to 15, leaving the minimum's rint(w/step) + 15
+    below 0 unless the code is clamped; symmetric: max|w|/step = 9.8, so the
+    largest codes need the clamp at 7."""
+    Wf = (rng.standard_normal((256, D_out)) * 0.02).astype(np.float32)
+    m = np.float32((21.0 if not sym else 9.8) * 2.0 ** -24)
+    frac = rng.random((128, D_out)).astype(np.float32)
+    Wf[:128] = -frac * m if not sym else (frac * 2 - 1) * m
+    Wf[0] = -m
+    return Wf
+
+
+def test_pack_zero_clamped_by_a_subnormal_step(awq):
+    """Codes on the group minimum where the zero is clamped at 15 (and, for
+    symmetric codes, where the largest |w|/step exceeds 7.5): both packs
+    bit-exact against the oracle, which clamps every code to [0, 15]."""
+    rng = np.random.default_rng(21)
+    D_out = 64
+    for sym in (False, True):
+        Wb = synth.to_bf16(_subnormal_step_groups(rng, D_out, sym))
+        Wf = synth.bf16_to_f32(Wb)
+        s = np.ones(256, dtype=np.float32)
+        oq, osc, oz = orc.pack(Wf, s, 128, sym)
+        if not sym:
+            assert np.all(oz.astype(np.float32)[0] == 15.0)
+        qw, sc, z = awq.quantize_pack(Wb.cuda(), torch.from_numpy(s).cuda(), 128, sym)
+        assert np.array_equal(qw.cpu().numpy(), oq)
+        assert np.array_equal(sc.cpu().numpy().view(np.uint16), osc.view(np.uint16))
+        assert np.array_equal(z.cpu().numpy().view(np.uint16), oz.view(np.uint16))
+        # the searched pack at s* = 1 (|x| = 1 everywhere, so s = 1 for every alpha)
+        Xb = synth.to_bf16(np.where(rng.random((64, 256)) < 0.5, -1.0, 1.0).astype(np.float32))
+        a = awq.act_stats(Xb.cuda())
+        res = awq.search(Xb.cuda(), Wb.cuda(), a, symmetric=sym)
+        assert np.all(res.s_star.cpu().numpy() == 1.0)
+        qw, sc, z = awq.quantize_pack_searched(Wb.cuda(), res, 128, sym)
+        assert np.array_equal(qw.cpu().numpy(), oq)
+        assert np.array_equal(z.cpu().numpy().view(np.uint16), oz.view(np.uint16))
