@@ -461,3 +461,31 @@ def check_closed_form_scales(orc):
 
 
 ALL_CHECKS.append(check_closed_form_scales)
+
+
+# ---------------------------------------------------------------- subnormal fp16 steps
+def check_subnormal_step_codes(orc, seed=14):
+    """Groups so small that the fp16 step is subnormal and rounds far below
+    the raw step (1.4 * 2^-24 -> 2^-24): a negative asymmetric group then has
+    -min/step = 21 and zero 15, a symmetric one max|w|/step = 9.8.  Every
+    code is still the nearest of the 16 (brute force), so the group minimum
+    takes the lowest code and the symmetric extremes +-7."""
+    rng = _rng(seed)
+    for sym in (False, True):
+        m = F32((9.8 if sym else 21.0) * 2.0 ** -24)
+        frac = rng.random((16, 6)).astype(F32)
+        Wp = (frac * 2 - 1) * m if sym else -frac * m
+        Wp[0] = -m
+        Wp = _bf16_round(Wp)
+        codes, step, zero = orc.quantize_groups(Wp, 16, sym)
+        assert np.all(step == F32(2.0 ** -24)), step
+        if not sym:
+            assert np.all(zero == 15.0) and np.all(-Wp[0] / step[0] > 15.5)
+        lo, hi = (1, 15) if sym else (0, 15)
+        for j in range(Wp.shape[0]):
+            for n in range(Wp.shape[1]):
+                assert int(codes[j, n]) == _nearest_code(Wp[j, n], step[0, n], zero[0, n], lo, hi), (sym, j, n)
+        assert np.all(codes[0] == lo)
+
+
+ALL_CHECKS.append(check_subnormal_step_codes)

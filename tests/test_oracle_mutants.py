@@ -56,6 +56,8 @@ MUTANTS = [
     ("closed_form_no_abs", "den = np.abs(W64).sum(axis=1) / W64.shape[1]", "den = np.abs(W64.sum(axis=1)) / W64.shape[1]"),
     ("closed_form_alpha_on_both", "s = np.where(den > 0, num / np.where(den > 0, den, 1.0), 1.0)",
      "s = np.where(den > 0, num / np.power(np.where(den > 0, den, 1.0), alpha), 1.0)"),
+    ("asym_no_lower_clamp", "q = np.clip(q, 0, qmax)", "q = np.minimum(q, qmax)"),
+    ("sym_no_clamp", "q = np.clip(q, -qmax, qmax)", "q = q"),
     ("alpha_scaled_twice", "return np.power(a.astype(np.float64), np.float64(alpha)).astype(F32)",
      "return np.power(a.astype(np.float64), np.float64(2 * alpha)).astype(F32)"),
 ]
