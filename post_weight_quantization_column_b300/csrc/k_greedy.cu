@@ -72,10 +72,10 @@ __device__ __forceinline__ Quant quant_of(Range r, uint32_t* status) {
 }
 
 // a * (w'hat / s - w)^2 for one weight w with scale s and rs = 1/s (powers of
-// two).  The fast form takes rint(w' * (1/step)) and raises `dev` to the
-// distance of that product from its rounding; where dev ends above the tie
-// guard the caller redoes the column with the exact form (rint of the IEEE
-// quotient).
+// two), with both clamps: the term of channel j under a candidate scale.
+// The fast form takes rint(w' * (1/step)) and raises `dev` to the distance
+// of that product from its rounding; where dev ends above the tie guard the
+// caller redoes the term with the exact form (rint of the IEEE quotient).
 template <bool SYM, bool EXACT>
 __device__ __forceinline__ float term(float w, float s, float rs, float a, Quant q, float& dev) {
   float d;
