@@ -213,3 +213,21 @@ def test_pack_zero_clamped_by_a_subnormal_step(awq):
         qw, sc, z = awq.quantize_pack_searched(Wb.cuda(), res, 128, sym)
         assert np.array_equal(qw.cpu().numpy(), oq)
         assert np.array_equal(z.cpu().numpy().view(np.uint16), oz.view(np.uint16))
+
+
+def test_pack_takes_s_at_a_4_byte_offset(awq):
+    """awq_quantize_pack reads s with plain loads: any 4-byte aligned s works
+    (here a view one float into a buffer), with results equal to the oracle's."""
+    w, X, W, Xf, Wf = _layer(34, D_in=256, D_out=136)
+    rng = np.random.default_rng(34)
+    s = (rng.random(256) * 3 + 0.25).astype(np.float32)
+    buf = torch.zeros(257, dtype=torch.float32, device="cuda")
+    buf[1:] = torch.from_numpy(s).cuda()
+    sv = buf[1:]
+    assert sv.data_ptr() % 16 == 4
+    for sym in (False, True):
+        qw, sc, z = awq.quantize_pack(W.cuda(), sv, 128, sym)
+        oq, osc, oz = orc.pack(Wf, s, 128, sym)
+        assert np.array_equal(qw.cpu().numpy(), oq)
+        assert np.array_equal(sc.cpu().numpy().view(np.uint16), osc.view(np.uint16))
+        assert np.array_equal(z.cpu().numpy().view(np.uint16), oz.view(np.uint16))
