@@ -93,7 +93,9 @@ __device__ __forceinline__ float maxabs3(float a, float b, float c) {
 // its columns to the exact path (see has_zero15).
 // inv, zmz: 1/step and 1.5*2^23 + the stored offset (the zero; 8 for
 // symmetric codes) of the 8 columns; out[p]: the 8 bytes of row pair p.
-template <bool SYM>
+// CLAMP = false drops the upper clamp (and the symmetric lower one) for
+// columns whose largest code is known to stay in range.
+template <bool SYM, bool CLAMP = true>
 __device__ __forceinline__ float codes_8x8(const uint4 (&w)[kPackRows], const float (&sj)[kPackRows],
                                            const float (&inv)[8], const float (&zmz)[8],
                                            uint32_t (&out)[kPackRows / 2][2]) {
@@ -120,16 +122,18 @@ __device__ __forceinline__ float codes_8x8(const uint4 (&w)[kPackRows], const fl
       const float2 dd = __ffma2_rn(po, ninv2, __fadd2_rn(co, nzm2));
       tmax = maxabs3(tmax, de.x, de.y);
       tmax = maxabs3(tmax, dd.x, dd.y);
-      if (SYM) {
+      if (SYM && CLAMP) {
         ce.x = fmaxf(ce.x, clo);
         ce.y = fmaxf(ce.y, clo);
         co.x = fmaxf(co.x, clo);
         co.y = fmaxf(co.y, clo);
       }
-      ce.x = fminf(ce.x, chi);
-      ce.y = fminf(ce.y, chi);
-      co.x = fminf(co.x, chi);
-      co.y = fminf(co.y, chi);
+      if (CLAMP) {
+        ce.x = fminf(ce.x, chi);
+        ce.y = fminf(ce.y, chi);
+        co.x = fminf(co.x, chi);
+        co.y = fminf(co.y, chi);
+      }
       const uint32_t x0 = __float_as_uint(co.x) * 16u + __float_as_uint(ce.x);  // byte 2j in the low 8 bits
       const uint32_t x1 = __float_as_uint(co.y) * 16u + __float_as_uint(ce.y);  // byte 2j+1
       half16[j] = __byte_perm(x0, x1, 0x0040);
@@ -230,6 +234,7 @@ __global__ void __launch_bounds__(kPackThreads, 3)
   __shared__ __align__(16) float red_lo[SYM ? 1 : P::WARPS][P::CW * kRangePad];
   __shared__ __align__(16) float red_hi[P::WARPS][P::CW * kRangePad];
   __shared__ __align__(16) float prm[P::GROUPS][P::CW * kQChunkFloats];  // the search table's chunk layout
+  __shared__ __align__(8) uint8_t clampc[P::GROUPS][P::COLS];  // 1: the column's codes need the clamps
 
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int c = lane % P::CW;
@@ -319,6 +324,14 @@ __global__ void __launch_bounds__(kPackThreads, 3)
     float z = 0.f;
     // an integer code in [0, 15]; the int round trip also turns -0 into +0
     if (!SYM && sc != 0.f) z = static_cast<float>(static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(-l, sc)), 0.f), 15.f)));
+    // Every element lies in [l, h], and rint is monotone, so outside near
+    // ties (the exact path) the largest code is rint(h/step) + zero
+    // (asymmetric) or rint(max|w'|/step) + 8 with max|w'| < 7.5 step
+    // (symmetric; 7.5 step is exact for an fp16 step).  Columns where that
+    // can leave the code range, and non-finite ones, keep the clamps.
+    bool need = !isfinite(l) || !isfinite(h);
+    if (sc != 0.f) need = need || (SYM ? h >= 7.5f * sc : rintf(__fdiv_rn(h, sc)) + z > 15.f);
+    clampc[g2][col] = need ? 1 : 0;
     float* q = &prm[g2][(col >> 3) * kQChunkFloats + (col & 7)];
     q[0] = sc != 0.f ? __frcp_rn(sc) : 0.f;
     q[kQChunkCols] = kMagic + (SYM ? 8.f : z);
@@ -345,7 +358,10 @@ __global__ void __launch_bounds__(kPackThreads, 3)
     }
   }
   uint32_t out[kPackRows / 2][2];
-  if (codes_8x8<SYM>(w, sj, inv, zmz, out) > kTieGuard || has_zero15<SYM>(zmz)) {
+  const uint2 cf = *reinterpret_cast<const uint2*>(&clampc[gi][c * kQChunkCols]);
+  const float tmax = (cf.x | cf.y) ? codes_8x8<SYM, true>(w, sj, inv, zmz, out)
+                                   : codes_8x8<SYM, false>(w, sj, inv, zmz, out);
+  if (tmax > kTieGuard || has_zero15<SYM>(zmz)) {
     pack_exact_8x8<SYM>(W, s, qc, row0, n, D_out, qweight);
     return;
   }
