@@ -31,7 +31,6 @@ std::mutex g_mu;
 int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
 int g_pairs[kMaxDevices];    // resident CTA pairs of the fused search (0 = not queried)
 int g_w4a16_pairs[kMaxDevices];  // resident CTA pairs of the W4A16 product (0 = not queried)
-int g_sms[kMaxDevices];      // multiprocessor count (0 = not queried)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 awq_status check_device(int* dev_out) {
@@ -67,17 +66,6 @@ awq_status get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 }
 
 awq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA; }
-
-awq_status get_sms(int dev, int* sms) {
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_sms[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return AWQ_ERR_CUDA;
-    g_sms[dev] = n;
-  }
-  *sms = g_sms[dev];
-  return AWQ_OK;
-}
 
 awq_status get_w4a16_pairs(int dev, int* pairs) {
   std::lock_guard<std::mutex> lk(g_mu);
