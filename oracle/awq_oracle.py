@@ -31,7 +31,9 @@ design notes of the repository):
      scale reproduces them ([adr] 关键设计 3: search and pack share one
      quantiser).
   R6 a step of 0 gives codes 0 (zero point 0) and dequantised value 0; a step
-     that overflows fp16 is an error.
+     that overflows fp16 is an error.  A subnormal fp16 step can round well
+     below range/15 (or max/7); the codes of R3 / R4 are then decided by
+     their clamps (a zero clamped at 15, symmetric codes at +-7).
   R7 loss is the plain sum of squares ||X S^-1 W'hat - X W||^2 (no mean),
      evaluated in the equivalent difference form X (S^-1 W'hat - W).
   R8 argmin takes the first index on ties.
