@@ -108,6 +108,9 @@ def test_calls_validate_before_cuda(L):
     assert L.awq_quantize_pack(fake, fake, 200, 256, ctypes.byref(cfg), fake, fake, fake, fake, 256, None) == 2
     assert L.awq_quantize_pack(fake, fake, 256, 256, ctypes.byref(cfg), ctypes.c_void_p(0x1001), fake, fake, fake,
                                256, None) == 3
+    # s needs 4-byte alignment: at +2 it is refused
+    assert L.awq_quantize_pack(fake, ctypes.c_void_p(0x1002), 256, 256, ctypes.byref(cfg), fake, fake, fake, fake,
+                               256, None) == 3
     # pack after a search: grid size out of range, group does not divide D_in,
     # misaligned s_star, workspace without the parameter table; empty is a no-op
     ps = L.awq_quantize_pack_searched
