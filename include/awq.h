@@ -348,9 +348,11 @@ AWQ_API awq_status awq_greedy_search(const void* W, const float* mean_abs, int64
  * zero) * scale) * RN(1/s_j)) and the products accumulate in fp32.  M <= 4
  * (decode): CUDA cores read each code once and form, per group, scale *
  * (sum_j x'_j code_j - zero * sum_j x'_j) with x' = fp32(x / s) and fp32
- * sums, the row blocks added in a fixed order in fp64.  Y is rounded to bf16.  Shapes: D_in a multiple of 64 and of group_size, D_out a multiple of
- * 16; all pointers 16-byte aligned (ws 256).  M = 0 is a no-op.  A timeout
- * of the kernel's bounded waits sets AWQ_ERR_TIMEOUT in the status word.
+ * sums, the row blocks added in a fixed order in fp64.  Y is rounded to
+ * bf16.  Shapes: D_in a multiple of 64 and of group_size, D_out a multiple
+ * of 16; all pointers 16-byte aligned (ws 256).  M = 0 is a no-op.  A
+ * timeout of the kernel's bounded waits sets AWQ_ERR_TIMEOUT in the status
+ * word.
  * ------------------------------------------------------------------------- */
 AWQ_API awq_status awq_w4a16_workspace_size(int64_t M, int64_t D_in, int64_t D_out, size_t* bytes);
 AWQ_API awq_status awq_w4a16_matmul(const void* X, int64_t M, int64_t D_in, int64_t D_out, const uint8_t* qweight,
