@@ -7,9 +7,11 @@ argmin, s*) -> quantize_pack_searched (int4 codes, fp16 scales / zeros, with
 the group parameters the search computed for alpha*).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload attn_proj]
+                    [--workload large_mlp] [--extras all|none|pack_any,w4a16,gram,greedy]
 
-Prints one JSON line.  `value` is the candidate-GEMM throughput of the whole
+The default layer is the largest one that the path is quoted on: X [16384 x
+8192], W [8192 x 28672], 4-bit symmetric, groups of 128, 21 alphas.  Prints
+one JSON line.  `value` is the candidate-GEMM throughput of the whole
 step, 21 * 2 * N * D_in * D_out flops divided by the step time (TFLOP/s),
 summed over ranks (each rank runs its own replica of the layer).  L2 is
 flushed (a 256 MiB write, then a 256 MiB read) before every timed step.  Under torchrun each rank
@@ -36,10 +38,12 @@ SEARCH_KERNELS = ("search_fused",)
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="attn_proj")
+    ap.add_argument("--workload", default="large_mlp")
+    ap.add_argument("--extras", default="all",
+                    help="measurements after the step: all, none, or a comma list of pack_any,w4a16,gram,greedy")
     ap.add_argument("--grid", type=int, default=21)
     ap.add_argument("--flush-mib", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -328,6 +332,112 @@ def run_reference(args, world, rank):
     return 0
 
 
+# ---------------------------------------------------------------------------- after-path measurements
+def _timed(fn, flush_l2, reps):
+    """CUDA-event times (ms) of `reps` calls of fn on the current stream, L2 flushed before each."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        flush_l2()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return sorted(a.elapsed_time(b) for a, b in ev)
+
+
+def measure_pack_any(awq, Wd, res, pk, g, sym, flush_l2, peaks, world):
+    """awq_quantize_pack at the step's s*: the pack for any s, which forms the
+    group ranges itself (separate from the step)."""
+    import torch
+    Di, Do = Wd.shape
+    pk2 = tuple(torch.empty_like(t) for t in pk)
+    ws_p = torch.empty(256, dtype=torch.uint8, device=Wd.device)
+    run = lambda: awq.quantize_pack(Wd, res.s_star, g, sym, out=pk2, ws=ws_p, check=False)  # noqa: E731
+    for _ in range(3):
+        run()
+    p_ms = max_over_ranks(_timed(run, flush_l2, 10)[5], world)
+    awq.check_workspace(ws_p, "pack")
+    same = all(torch.equal(a, b) for a, b in zip(pk, pk2))
+    p_bytes = 2.0 * Di * Do + 4.0 * Di + Di * Do / 2.0 + 4.0 * Do * Di / g
+    return {"workload": f"awq_quantize_pack(W, s*), D_in={Di} D_out={Do} g={g}", "us": p_ms * 1e3,
+            "bytes": p_bytes, "gbs": p_bytes / (p_ms * 1e-3) / 1e9,
+            "frac_hbm": p_bytes / (p_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "bound": "hbm",
+            "equals_searched_pack": same, "timing": "median of 10 launches, L2 flushed before each"}
+
+
+def measure_w4a16(awq, Xd, res, pk, g, flush_l2, peaks, world):
+    """The W4A16 product of the step's packed layer on the layer's own
+    activations, Y = (X diag(1/s*)) Dequant(qweight), and its one-row form."""
+    import torch
+    N, Di = Xd.shape
+    Do = pk[0].shape[1]
+    T = Di // g
+    Y = torch.empty(N, Do, dtype=torch.bfloat16, device=Xd.device)
+    ws_y = torch.empty(256, dtype=torch.uint8, device=Xd.device)
+    run = lambda: awq.w4a16_matmul(Xd, *pk, res.s_star, g, out=Y, ws=ws_y, check=False)  # noqa: E731
+    for _ in range(3):
+        run()
+    awq.check_workspace(ws_y, "w4a16")
+    y_ms = max_over_ranks(_timed(run, flush_l2, 10)[5], world)
+    awq.check_workspace(ws_y, "w4a16")
+    y_tf = 2.0 * N * Di * Do / (y_ms * 1e-3) / 1e12
+    w4 = {"workload": f"Y = (X diag(1/s*)) Dequant(qweight), M={N} D_in={Di} D_out={Do}, bf16 out",
+          "ms": y_ms, "tflops": y_tf, "bound": "tensor", "peak": peaks["bf16_tflops"],
+          "frac": y_tf / peaks["bf16_tflops"], "timing": "median of 10 launches, L2 flushed before each"}
+    del Y
+    # one row of X through the same packed layer: the decode path, bound by the code bytes
+    X1 = Xd[:1].contiguous()
+    Y1 = torch.empty(1, Do, dtype=torch.bfloat16, device=Xd.device)
+    ws_1 = torch.empty(awq.w4a16_workspace_size(1, Di, Do), dtype=torch.uint8, device=Xd.device)
+    run1 = lambda: awq.w4a16_matmul(X1, *pk, res.s_star, g, out=Y1, ws=ws_1, check=False)  # noqa: E731
+    for _ in range(3):
+        run1()
+    d_ms = max_over_ranks(_timed(run1, flush_l2, 10)[5], world)
+    awq.check_workspace(ws_1, "w4a16 decode")
+    d_bytes = Di * Do / 2 + 4.0 * T * Do + 2.0 * (Di + Do) + 4.0 * Di
+    w4["decode_m1"] = {"us": d_ms * 1e3, "bytes": d_bytes, "gbs": d_bytes / (d_ms * 1e-3) / 1e9,
+                       "frac_hbm": d_bytes / (d_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "bound": "hbm"}
+    return w4
+
+
+def measure_gram(awq, Xd, Wd, a_buf, grid, g, sym, ws_q, res, flush_l2, world):
+    """The same search through the Gram factor of X (N > D_in), against the direct search."""
+    import torch
+    N, Di = Xd.shape
+    Do = Wd.shape[1]
+    G = len(grid)
+    ws_g = torch.empty(awq.search_gram_workspace_size(N, Di, Do, G, g, sym), dtype=torch.uint8, device=Xd.device)
+    res_g = awq.SearchResult(torch.empty(G, dtype=torch.float64, device=Xd.device),
+                             torch.empty(1, dtype=torch.int32, device=Xd.device),
+                             torch.empty(Di, dtype=torch.float32, device=Xd.device), None, grid, ws_g)
+    awq.search(Xd, Wd, a_buf, grid, g, sym, ws=ws_g, out=res_g, gram=True)
+    awq.search(Xd, Wd, a_buf, grid, g, sym, ws=ws_q, out=res)
+    torch.cuda.synchronize()
+    tg = _timed(lambda: awq.search(Xd, Wd, a_buf, grid, g, sym, check=False, ws=ws_g, out=res_g, gram=True),
+                flush_l2, 3)
+    td = _timed(lambda: awq.search(Xd, Wd, a_buf, grid, g, sym, check=False, ws=ws_q, out=res), flush_l2, 3)
+    awq.check_workspace(ws_g, "search gram")
+    g_ms = max_over_ranks(tg[1], world)
+    d_ms = max_over_ranks(td[1], world)
+    rel = (res_g.losses - res.losses).abs().div(res.losses).max().item()
+    return {"workload": f"search through R = chol(X^T X)^T, {Di} rows instead of {N}", "ms": g_ms,
+            "direct_ms": d_ms, "speedup": d_ms / g_ms, "max_rel_loss_diff_vs_direct": rel,
+            "same_alpha_star": int(res_g.best_idx.item()) == int(res.best_idx.item()),
+            "timing": "median of 3 after one warm-up, L2 flushed before each"}
+
+
+def measure_greedy(awq, Wd, a_buf, g, sym, flush_l2, world):
+    """The adr's per-group coordinate greedy on the same layer."""
+    Di, Do = Wd.shape
+    t = _timed(lambda: awq.greedy_search(Wd, a_buf, g, sym, check=False), flush_l2, 3)
+    g_ms = max_over_ranks(t[0], world)
+    evals = 3.0 * Di * 20 * Do
+    return {"workload": f"adr greedy: 3 passes x 20 power-of-two candidates, D_in={Di} D_out={Do} g={g}",
+            "ms": g_ms, "candidate_column_evaluations": evals, "evals_per_s": evals / (g_ms * 1e-3),
+            "launches": 3 * g + 1, "timing": "best of 3, L2 flushed before each"}
+
+
 # ---------------------------------------------------------------------------- our arm
 def run_ours(args, world, rank, local):
     import numpy as np
@@ -346,6 +456,12 @@ def run_ours(args, world, rank, local):
     Xd, Wd = X.to(dev), W.to(dev)
     N, Di, Do, g, sym = w.N, w.D_in, w.D_out, w.group_size, w.symmetric
     T = Di // g
+    all_extras = ("pack_any", "w4a16", "gram", "greedy")
+    extras = set(all_extras) if args.extras == "all" else \
+        set() if args.extras == "none" else {e.strip() for e in args.extras.split(",") if e.strip()}
+    unknown = extras - set(all_extras)
+    if unknown:
+        raise SystemExit(f"unknown --extras entries: {sorted(unknown)}")
     a_buf = torch.empty(Di, dtype=torch.float32, device=dev)
     ws_s = torch.empty(awq.act_stats_workspace_size(N, Di), dtype=torch.uint8, device=dev)
     ws_q = torch.empty(awq.search_workspace_size(N, Di, Do, G, g, sym), dtype=torch.uint8, device=dev)
@@ -407,10 +523,21 @@ def run_ours(args, world, rank, local):
     stats_ms = per_launch_ms("act_stats")
     peaks, peak_src = measured_peaks()
     achieved = flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
+    # The burst peak is for a kernel timed on its own; a kernel timed inside a
+    # long loaded stretch (here: a timed region of a second or more) runs
+    # under the power cap and is held to the sustained peak.
+    timed_s = step_ms * args.steps * 1e-3
+    sustained = timed_s >= 1.0
+    peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     roofline = {"kernel": search_name, "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"] if achieved else None,
-                "traffic": None, "peak_source": f"{peak_src} bf16 dense burst",
+                "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak if achieved else None,
+                "traffic": None,
+                "peak_source": (f"{peak_src} bf16 dense "
+                                + (f"sustained (timed region {timed_s:.1f} s under load)" if sustained
+                                   else f"burst (timed region {timed_s:.2f} s)")),
+                "frac_of_burst": achieved / peaks["bf16_tflops"] if achieved else None,
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"] if achieved else None,
                 "algorithmic": f"2*N*D_in*D_out*G = {flops:.4g} flop per launch"}
     tp = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
     if os.path.exists(tp):
@@ -450,115 +577,25 @@ def run_ours(args, world, rank, local):
 
     # ---- awq_quantize_pack at the step's s* on its own: the pack for any s,
     # which also forms the group ranges (separate from the step)
-    pk2 = tuple(torch.empty_like(t) for t in pk)
-    ws_p = torch.empty(256, dtype=torch.uint8, device=dev)
-    for _ in range(3):
-        awq.quantize_pack(Wd, res.s_star, g, sym, out=pk2, ws=ws_p, check=False)
-    p_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
-    for i in range(10):
-        flush_l2()
-        p_ev[i][0].record()
-        awq.quantize_pack(Wd, res.s_star, g, sym, out=pk2, ws=ws_p, check=False)
-        p_ev[i][1].record()
-    torch.cuda.synchronize()
-    awq.check_workspace(ws_p, "pack")
-    same = all(torch.equal(a, b) for a, b in zip(pk, pk2))
-    p_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in p_ev)[5], world)
-    p_bytes = 2.0 * Di * Do + 4.0 * Di + Di * Do / 2.0 + 4.0 * Do * Di / g
-    pack_any = {"workload": f"awq_quantize_pack(W, s*), D_in={Di} D_out={Do} g={g}", "us": p_ms * 1e3,
-                "bytes": p_bytes, "gbs": p_bytes / (p_ms * 1e-3) / 1e9,
-                "frac_hbm": p_bytes / (p_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "bound": "hbm",
-                "equals_searched_pack": same, "timing": "median of 10 launches, L2 flushed before each"}
-    del pk2
+    pack_any = None
+    if "pack_any" in extras:
+        pack_any = measure_pack_any(awq, Wd, res, pk, g, sym, flush_l2, peaks, world)
 
     # ---- after the path: the W4A16 product of the step's packed layer on its
     # own activations, Y = (X diag(1/s*)) Dequant(qweight); separate from the step
     w4 = None
-    if Do % 16 == 0 and Di % 64 == 0:
-        Y = torch.empty(N, Do, dtype=torch.bfloat16, device=dev)
-        ws_y = torch.empty(256, dtype=torch.uint8, device=dev)
-        for _ in range(3):
-            awq.w4a16_matmul(Xd, *pk, res.s_star, g, out=Y, ws=ws_y, check=False)
-        awq.check_workspace(ws_y, "w4a16")
-        y_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
-        for i in range(10):
-            flush_l2()
-            y_ev[i][0].record()
-            awq.w4a16_matmul(Xd, *pk, res.s_star, g, out=Y, ws=ws_y, check=False)
-            y_ev[i][1].record()
-        torch.cuda.synchronize()
-        awq.check_workspace(ws_y, "w4a16")
-        y_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in y_ev)[5], world)
-        y_tf = 2.0 * N * Di * Do / (y_ms * 1e-3) / 1e12
-        w4 = {"workload": f"Y = (X diag(1/s*)) Dequant(qweight), M={N} D_in={Di} D_out={Do}, bf16 out",
-              "ms": y_ms, "tflops": y_tf, "bound": "tensor", "peak": peaks["bf16_tflops"],
-              "frac": y_tf / peaks["bf16_tflops"], "timing": "median of 10 launches, L2 flushed before each"}
-        del Y
-        # one row of X through the same packed layer: the decode path, bound by the code bytes
-        X1 = Xd[:1].contiguous()
-        Y1 = torch.empty(1, Do, dtype=torch.bfloat16, device=dev)
-        ws_1 = torch.empty(awq.w4a16_workspace_size(1, Di, Do), dtype=torch.uint8, device=dev)
-        for _ in range(3):
-            awq.w4a16_matmul(X1, *pk, res.s_star, g, out=Y1, ws=ws_1, check=False)
-        d_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
-        for i in range(10):
-            flush_l2()
-            d_ev[i][0].record()
-            awq.w4a16_matmul(X1, *pk, res.s_star, g, out=Y1, ws=ws_1, check=False)
-            d_ev[i][1].record()
-        torch.cuda.synchronize()
-        awq.check_workspace(ws_1, "w4a16 decode")
-        d_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in d_ev)[5], world)
-        d_bytes = Di * Do / 2 + 4.0 * T * Do + 2.0 * (Di + Do) + 4.0 * Di
-        w4["decode_m1"] = {"us": d_ms * 1e3, "bytes": d_bytes, "gbs": d_bytes / (d_ms * 1e-3) / 1e9,
-                           "frac_hbm": d_bytes / (d_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "bound": "hbm"}
+    if "w4a16" in extras and Do % 16 == 0 and Di % 64 == 0:
+        w4 = measure_w4a16(awq, Xd, res, pk, g, flush_l2, peaks, world)
 
     # ---- the same search through the Gram factor of X, where N > D_in (separate from the step)
     gram = None
-    if N > Di and Di % 64 == 0:
-        ws_g = torch.empty(awq.search_gram_workspace_size(N, Di, Do, G, g, sym), dtype=torch.uint8, device=dev)
-        res_g = awq.SearchResult(torch.empty(G, dtype=torch.float64, device=dev),
-                                 torch.empty(1, dtype=torch.int32, device=dev),
-                                 torch.empty(Di, dtype=torch.float32, device=dev), None, grid, ws_g)
-        awq.search(Xd, Wd, a_buf, grid, g, sym, ws=ws_g, out=res_g, gram=True)
-        awq.search(Xd, Wd, a_buf, grid, g, sym, ws=ws_q, out=res)
-        torch.cuda.synchronize()
-        tg, td = [], []
-        for i in range(3):
-            for lst, kw in ((tg, dict(ws=ws_g, out=res_g, gram=True)), (td, dict(ws=ws_q, out=res))):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                flush_l2()
-                e0.record()
-                awq.search(Xd, Wd, a_buf, grid, g, sym, check=False, **kw)
-                e1.record()
-                lst.append((e0, e1))
-        torch.cuda.synchronize()
-        awq.check_workspace(ws_g, "search gram")
-        g_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in tg)[1], world)
-        d_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in td)[1], world)
-        rel = (res_g.losses - res.losses).abs().div(res.losses).max().item()
-        gram = {"workload": f"search through R = chol(X^T X)^T, {Di} rows instead of {N}", "ms": g_ms,
-                "direct_ms": d_ms, "speedup": d_ms / g_ms, "max_rel_loss_diff_vs_direct": rel,
-                "same_alpha_star": int(res_g.best_idx.item()) == int(res.best_idx.item()),
-                "timing": "median of 3 after one warm-up, L2 flushed before each"}
-        del ws_g
+    if "gram" in extras and N > Di and Di % 64 == 0:
+        gram = measure_gram(awq, Xd, Wd, a_buf, grid, g, sym, ws_q, res, flush_l2, world)
 
     # ---- the adr's greedy search on the same layer (separate from the step)
     gr = None
-    g_ev = []
-    for i in range(3):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        flush_l2()
-        e0.record()
-        awq.greedy_search(Wd, a_buf, g, sym, check=False)
-        e1.record()
-        g_ev.append((e0, e1))
-    torch.cuda.synchronize()
-    g_ms = max_over_ranks(sorted(a.elapsed_time(b) for a, b in g_ev[1:])[0], world)
-    evals = 3.0 * Di * 20 * Do
-    gr = {"workload": f"adr greedy: 3 passes x 20 power-of-two candidates, D_in={Di} D_out={Do} g={g}",
-          "ms": g_ms, "candidate_column_evaluations": evals, "evals_per_s": evals / (g_ms * 1e-3),
-          "launches": 3 * g + 1, "timing": "best of 2 after one warm-up, L2 flushed before each"}
+    if "greedy" in extras:
+        gr = measure_greedy(awq, Wd, a_buf, g, sym, flush_l2, world)
     for ws, nm in ((ws_s, "act_stats"), (ws_q, "search")):
         awq.check_workspace(ws, nm)
 

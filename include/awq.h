@@ -153,24 +153,29 @@ AWQ_API awq_status awq_act_stats_finalize(const double* sum_abs, int64_t rows, i
  * host program that has already reserved all device memory for its own pool
  * and exposes no allocator, or code on a latency-critical path that must not
  * call cudaMalloc (which can synchronise the whole device).  This entry point
- * takes only X and the output; its scratch (the per-row-slice partial sums
- * and one completion counter per 256 channels) is a 4 MiB + 16 KiB array of
- * static device memory inside the library, which every device that loads the
- * library holds until the process exits.  Each call clears the counters it
- * uses (cudaMemsetAsync on the array, which allocates nothing).
+ * takes only X and the output; its scratch (a status word, one completion
+ * counter per 256 channels and the per-row-slice partial sums) is a
+ * 256 B + 16 KiB + 4 MiB array of static device memory inside the library,
+ * which every device that loads the library holds until the process exits.
+ * Each call clears the status word and the counters it uses
+ * (cudaMemsetAsync on the array, which allocates nothing).
  *
  *   X, N, D_in, ldx, mean_abs  as for awq_act_stats
- * Limits: D_in <= 1048576 channels (one row slice must fit the array);
- * larger D_in returns AWQ_ERR_SHAPE without launching anything.  The call
- * makes no cudaMalloc / cudaFree and uses no allocating library routine.
- * The first call on a device looks up the array's device address for that
- * device (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture.  Every call shares the one array: calls
- * whose kernels overlap on the GPU (e.g. on two streams) race and corrupt
- * each other's result, so serialise them.  Results equal awq_act_stats'
- * whenever its row-slice plan fits the array, and agree to rounding
- * otherwise.  There is no device status word: a non-finite X shows up as a
- * non-finite entry of mean_abs.
+ * Limits: D_in <= 1048576 channels; larger D_in returns AWQ_ERR_SHAPE without
+ * launching anything.  The call makes no cudaMalloc / cudaFree and uses no
+ * allocating library routine.  The first call on a device looks up the
+ * array's device address for that device (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture.  The
+ * address is kept per device and CUDA context: after cudaDeviceReset the next
+ * call looks it up again in the new context (again a first call, to be made
+ * outside a capture).  Every call shares the one array: calls whose kernels
+ * overlap on the GPU (e.g. on two streams) race and corrupt each other's
+ * result, so serialise them.  Results are bit-identical to awq_act_stats'
+ * (same row-slice plan, same kernel, same summation order).  There is no
+ * status word for the caller to read, so device-side failures show up in the
+ * output: a non-finite X gives a non-finite entry of mean_abs, and a bounded
+ * device wait that expires (AWQ_ERR_TIMEOUT in the other entry points) makes
+ * the means of the affected 256-channel chunk NaN.
  * ------------------------------------------------------------------------- */
 AWQ_API awq_status awq_act_stats_noalloc(const void* X, int64_t N, int64_t D_in, int64_t ldx,
                                          float* mean_abs, awq_stream_t stream);

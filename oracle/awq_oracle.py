@@ -13,8 +13,7 @@ Sources (page title, then section):
   [adr]      "009. AWQ Integration" (ADR), Decision / 关键设计
   [glossary] "量化推理算法 GPTQ / AWQ" (slowleelab), L4 section 4.1 / 4.3
 
-Readings where the pages are silent or disagree (each is also listed in the
-design notes of the repository):
+Readings where the pages are silent or disagree:
   R1 statistic is mean|X_j| (the concept page also mentions max; the aiqz
      article and the ADR use the mean of absolute values).
   R2 the scale exponent grid is alpha_k = k/(G-1), computed in float64, and the

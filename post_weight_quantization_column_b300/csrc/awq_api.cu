@@ -280,7 +280,7 @@ awq_status run_act_stats(const void* X, int64_t N, int64_t D_in, int64_t ldx, fl
   float* partial_max = reinterpret_cast<float*>(base + kHeaderBytes + tb + stats_partial_bytes(N, D_in));
   ProfScope prof(name, s);
   return from_cuda(launch_act_stats(encode, X, N, D_in, ldx, mean_abs, sum_abs, max_abs, partial, partial_max,
-                                    tickets, splits, rps, status_word(ws), s));
+                                    tickets, splits, rps, status_word(ws), 0, s));
 }
 }  // namespace
 

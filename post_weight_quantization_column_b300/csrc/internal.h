@@ -23,11 +23,13 @@ void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split);
 // Column chunks of 256 channels: the number of ticket counters the kernel uses.
 int64_t stats_chunks(int64_t D);
 // partial: fp32 [splits][D] scratch; tickets: uint32 [stats_chunks(D)], zero on
-// entry (the kernel leaves them zero again).
+// entry (the kernel leaves them zero again).  nan_on_error: means of a chunk
+// are written as NaN when the status word is non-zero once its slices are in
+// (for a status word the caller never reads).
 cudaError_t launch_act_stats(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, int64_t N, int64_t D,
                              int64_t ldx, float* mean_abs, double* sum_abs, float* max_abs, float* partial,
                              float* partial_max, unsigned int* tickets, int splits, int64_t rows_per_split,
-                             uint32_t* status, cudaStream_t stream);
+                             uint32_t* status, int nan_on_error, cudaStream_t stream);
 cudaError_t launch_stats_finalize(const double* sum_abs, int64_t rows, int64_t D, float* mean_abs,
                                   cudaStream_t stream);
 // The driver's tensor-map encoder (resolved once per process).

@@ -63,7 +63,10 @@ __device__ __forceinline__ void add_vec(const uint4& v, float (&acc)[8], float (
 
 // mean_abs: written with the mean when sum_abs is null.  sum_abs: when given,
 // the slice total of each channel (float64) is added to it instead.  max_abs:
-// when kMax, max(max_abs, the batch's max |x|) is stored back.
+// when kMax, max(max_abs, the batch's max |x|) is stored back.  nan_on_error:
+// the last CTA of a chunk writes NaN means when the status word is set (a row
+// slice of the chunk gave up a wait and its partial sums are incomplete), for
+// callers that have no status word of their own to read.
 template <bool kMax>
 __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_constant__ CUtensorMap tmX, int64_t N,
                                                                  int64_t D, int64_t rows_per_split,
@@ -72,7 +75,8 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_c
                                                                  unsigned int* __restrict__ tickets,
                                                                  float* __restrict__ mean_abs,
                                                                  double* __restrict__ sum_abs,
-                                                                 float* __restrict__ max_abs, uint32_t* status) {
+                                                                 float* __restrict__ max_abs, uint32_t* status,
+                                                                 int nan_on_error) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(16) float red[kStatsRowLanes][kStatsCols];
   __shared__ __align__(8) uint64_t full_bar[kStatsStages];
@@ -186,6 +190,8 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_c
   __syncthreads();
   if (!last) return;
   __threadfence();
+  // a slice that timed out set the status word before its ticket
+  const bool poison = nan_on_error && status && *reinterpret_cast<volatile uint32_t*>(status) != 0u;
   if (t < kStatsCols && t < width) {
     // the slices in order, 32 loads in flight per batch (one batch unless
     // the grid has more than 32 slices)
@@ -203,7 +209,7 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_c
     if (sum_abs) {
       sum_abs[j] += s;  // this CTA alone owns channel j now
     } else {
-      mean_abs[j] = static_cast<float>(s / static_cast<double>(N));
+      mean_abs[j] = poison ? __int_as_float(0x7FC00000) : static_cast<float>(s / static_cast<double>(N));
     }
     if (kMax) {
       float m = max_abs[j];
@@ -239,7 +245,7 @@ void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split) {
 cudaError_t launch_act_stats(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, int64_t N, int64_t D,
                              int64_t ldx, float* mean_abs, double* sum_abs, float* max_abs, float* partial,
                              float* partial_max, unsigned int* tickets, int splits, int64_t rows_per_split,
-                             uint32_t* status, cudaStream_t stream) {
+                             uint32_t* status, int nan_on_error, cudaStream_t stream) {
   CUtensorMap tm;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
@@ -255,13 +261,13 @@ cudaError_t launch_act_stats(PFN_cuTensorMapEncodeTiled_v12000 encode, const voi
                                          kStatsSmem);
     if (e != cudaSuccess) return e;
     act_stats_kernel<true><<<grid, kStatsThreads, kStatsSmem, stream>>>(
-        tm, N, D, rows_per_split, partial, partial_max, tickets, mean_abs, sum_abs, max_abs, status);
+        tm, N, D, rows_per_split, partial, partial_max, tickets, mean_abs, sum_abs, max_abs, status, nan_on_error);
   } else {
     cudaError_t e = cudaFuncSetAttribute(act_stats_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kStatsSmem);
     if (e != cudaSuccess) return e;
     act_stats_kernel<false><<<grid, kStatsThreads, kStatsSmem, stream>>>(
-        tm, N, D, rows_per_split, partial, partial_max, tickets, mean_abs, sum_abs, max_abs, status);
+        tm, N, D, rows_per_split, partial, partial_max, tickets, mean_abs, sum_abs, max_abs, status, nan_on_error);
   }
   return cudaGetLastError();
 }

@@ -53,7 +53,18 @@ def check_alpha_star(gpu_best: int, oracle_losses: np.ndarray, rtol=LOSS_RTOL):
     assert oracle_losses[gpu_best] <= oracle_losses[ob] * (1 + rtol), (gpu_best, ob, oracle_losses)
 
 
-def check_column_losses(got, want, rtol=LOSS_RTOL, min_frac=0.98):
+def record(kind: str, **fields):
+    """Append one JSON line to the file named by AWQ_TEST_RECORD, if set (a
+    record of measured agreement, e.g. the share of columns within rtol)."""
+    path = os.environ.get("AWQ_TEST_RECORD")
+    if not path:
+        return
+    import json
+    with open(path, "a") as f:
+        f.write(json.dumps({"kind": kind, **fields}) + "\n")
+
+
+def check_column_losses(got, want, rtol=LOSS_RTOL, min_frac=0.98, label=""):
     """Per-column losses: the search may round a code the other way where w'/step
     sits within ~1e-6 of a half step (reciprocal multiply instead of IEEE
     division), which moves that column's loss by a few percent.  Require most
@@ -63,6 +74,8 @@ def check_column_losses(got, want, rtol=LOSS_RTOL, min_frac=0.98):
     big = want > 1e-3 * want.max()
     e = rel_err(got[big], want[big])
     frac = float(np.mean(e <= rtol))
+    record("column_losses", label=label, columns=int(e.size), outside=int(np.count_nonzero(e > rtol)),
+           frac_within=frac, max_rel=float(e.max()))
     assert frac >= min_frac, (frac, float(e.max()))
     assert e.max() <= 0.25, float(e.max())
     return frac, float(e.max())

@@ -489,3 +489,28 @@ def check_subnormal_step_codes(orc, seed=14):
 
 
 ALL_CHECKS.append(check_subnormal_step_codes)
+
+
+# ---------------------------------------------------------------- relative error (aiqz section 5)
+def check_relative_error_hand(orc):
+    """epsilon = ||X (W - W_hat)||^2 / ||X W||^2 on a 2 x 2 case worked by
+    hand: X W = [[3, 2], [7, 4]], whose squares sum to 9 + 4 + 49 + 16 = 78, so
+    a loss of 39 is epsilon = 1/2 and a loss of 78 is 1.  The loss itself is
+    the search's, and a quantised layer's epsilon is its loss over the same
+    energy (checked against a product formed element by element)."""
+    X = np.array([[1.0, 2.0], [3.0, 4.0]], dtype=F32)
+    W = np.array([[1.0, 0.0], [1.0, 1.0]], dtype=F32)
+    assert orc.relative_error(X, W, 39.0) == 0.5
+    assert orc.relative_error(X, W, 78.0) == 1.0
+    Xs, Ws = small_layer(21, N=8, D_in=16, D_out=4)
+    res = orc.search(Xs, Ws, orc.act_stats(Xs), orc.alpha_grid(3), group_size=8, symmetric=True)
+    energy = 0.0
+    for r in range(Xs.shape[0]):
+        for n in range(Ws.shape[1]):
+            y = sum(float(Xs[r, j]) * float(Ws[j, n]) for j in range(Xs.shape[1]))
+            energy += y * y
+    for L in res["losses"]:
+        assert abs(orc.relative_error(Xs, Ws, float(L)) - float(L) / energy) <= 1e-12 * float(L) / energy
+
+
+ALL_CHECKS.append(check_relative_error_hand)

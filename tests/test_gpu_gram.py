@@ -40,7 +40,7 @@ def test_gram_search_matches_oracle(awq, w):
     check_alpha_star(res.best, ref["losses"])
     s_star = res.s_star.cpu().numpy()
     assert np.array_equal(s_star, orc.scales(a, grid[res.best]))
-    check_column_losses(res.col_losses.cpu().numpy(), ref["col_losses"])
+    check_column_losses(res.col_losses.cpu().numpy(), ref["col_losses"], label=f"gram {w.name}")
     # the searched pack reads the group parameters from the same workspace
     qw, sc, z = awq.quantize_pack_searched(Wd, res, w.group_size, w.symmetric)
     oq, osc, oz = orc.pack(Wf, s_star, w.group_size, w.symmetric)
@@ -65,7 +65,7 @@ def test_gram_search_full_size_sampled(awq):
     torch.cuda.empty_cache()
     cols = synth.sample_columns(w.D_out, 512, w.seed)
     ref = orc.search(Xf, Wf, a, grid, group_size=w.group_size, symmetric=w.symmetric, cols=cols)
-    check_column_losses(col[:, cols], ref["col_losses"])
+    check_column_losses(col[:, cols], ref["col_losses"], label="gram sampled")
     np.testing.assert_allclose(col.sum(axis=1), L, rtol=1e-9)
 
 

@@ -119,7 +119,7 @@ def _search_full_check(awq, w, X, W, Xf, Wf):
     s_star = res.s_star.cpu().numpy()
     assert np.array_equal(s_star, orc.scales(a, grid[res.best]))
     col = res.col_losses.cpu().numpy()
-    check_column_losses(col, ref["col_losses"])
+    check_column_losses(col, ref["col_losses"], label=w.name)
     np.testing.assert_allclose(col.sum(axis=1), L, rtol=1e-9)
     print(f"{w.name}: max per-alpha rel err {rel_err(L, ref['losses']).max():.3e}, best {res.best} / {ref['best']}")
     return res, ref
@@ -157,7 +157,7 @@ def test_search_full_size_sampled_columns(awq, name):
     err = rel_err(got.sum(axis=1), ref["losses"]).max()
     print(f"{name}: sampled per-alpha rel err {err:.3e}")
     assert err <= LOSS_RTOL
-    check_column_losses(got, ref["col_losses"])
+    check_column_losses(got, ref["col_losses"], label=f"{name} ({len(cols)} sampled columns)")
     np.testing.assert_allclose(col.sum(axis=1), L, rtol=1e-9)
     assert res.best == int(np.argmin(L))
     assert np.array_equal(res.s_star.cpu().numpy(), orc.scales(a, grid[res.best]))

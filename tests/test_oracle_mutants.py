@@ -60,6 +60,11 @@ MUTANTS = [
     ("sym_no_clamp", "q = np.clip(q, -qmax, qmax)", "q = q"),
     ("alpha_scaled_twice", "return np.power(a.astype(np.float64), np.float64(alpha)).astype(F32)",
      "return np.power(a.astype(np.float64), np.float64(2 * alpha)).astype(F32)"),
+    ("epsilon_over_weight_energy", "return float(loss / (Y * Y).sum())",
+     "return float(loss / (np.asarray(W, dtype=np.float64) ** 2).sum())"),
+    ("epsilon_transposed_weight", "Y = np.asarray(X, dtype=np.float64) @ np.asarray(W, dtype=np.float64)",
+     "Y = np.asarray(X, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T"),
+    ("epsilon_not_squared", "return float(loss / (Y * Y).sum())", "return float(loss / np.abs(Y).sum())"),
 ]
 
 
