@@ -47,11 +47,14 @@ struct QParam {
   float inv, zm, step, pad;
 };
 // In memory they are stored per (candidate, group) in chunks of 8 output
-// columns: {inv x8, zm x8, step x8, 4 unused} = 28 floats (112 bytes).  The
+// columns: {inv x8, zm x8, step x8, clamp, 3 unused} = 28 floats (112 bytes).
+// clamp is 1.0 when some code of the chunk's 8 columns would leave the code
+// range without the clamps (else 0.0), so readers may drop them.  The
 // 112-byte stride spreads the 8 chunks read by 8 neighbouring producer
 // threads over all 32 shared-memory banks.
 constexpr int kQChunkCols = 8;
 constexpr int kQChunkFloats = 28;
+constexpr int kQChunkClamp = 3 * kQChunkCols;  // float index of the chunk's clamp flag
 inline size_t qparam_floats(int G, int64_t T, int64_t D_out) {
   return static_cast<size_t>(G) * static_cast<size_t>(T) * static_cast<size_t>(D_out / kQChunkCols) * kQChunkFloats;
 }

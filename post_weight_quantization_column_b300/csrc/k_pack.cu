@@ -27,6 +27,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -359,8 +361,8 @@ __global__ void __launch_bounds__(kPackThreads, 3)
   }
   uint32_t out[kPackRows / 2][2];
   const uint2 cf = *reinterpret_cast<const uint2*>(&clampc[gi][c * kQChunkCols]);
-  const float tmax = (cf.x | cf.y) ? codes_8x8<SYM, true>(w, sj, inv, zmz, out)
-                                   : codes_8x8<SYM, false>(w, sj, inv, zmz, out);
+  const bool clampw = __any_sync(__activemask(), (cf.x | cf.y) != 0u);  // one path per warp
+  const float tmax = clampw ? codes_8x8<SYM, true>(w, sj, inv, zmz, out) : codes_8x8<SYM, false>(w, sj, inv, zmz, out);
   if (tmax > kTieGuard || has_zero15<SYM>(zmz)) {
     pack_exact_8x8<SYM>(W, s, qc, row0, n, D_out, qweight);
     return;
@@ -383,30 +385,32 @@ cudaError_t launch_pack_t(const void* W, const float* s, int64_t D_in, int64_t D
 // ---------------------------------------------------------------------------
 // Pack after a search.  The search's group-parameter pass already holds, for
 // every candidate, the exact step (fp16-rounded range / 15 or max|w'| / 7),
-// 1/step and zero of every (group, column) -- the same formulas and the same
-// exact ranges as pack_kernel forms.  For its best candidate the pack is then
-// a single streaming pass with no exchange between threads: thread t of the
-// grid owns 8 columns (chunk c, fastest, so that a warp reads 512 contiguous
-// bytes of a row) x 8 rows of one group, loads all 8 rows at once and emits
-// codes as pack_kernel does; the threads of row block 0 write the group's
-// fp16 scales and zeros.
+// 1/step, zero and clamp flag of every (group, column) -- the same formulas
+// and the same exact ranges as pack_kernel forms.  For its best candidate the
+// pack is then a single streaming pass with no exchange between threads: a
+// thread owns 8 columns (chunk c) x 8 rows (row block rb) of one group, loads
+// all 8 rows at once and emits codes as pack_kernel does; the threads of row
+// block 0 of a group write its fp16 scales and zeros.  Grid: x = blocks of
+// 256 chunks (a warp reads 512 contiguous bytes of a row), y = row blocks
+// (strided over when there are more than the grid's y extent), so a thread
+// finds its place without divisions.
 template <int GS, bool SYM>
 __global__ void __launch_bounds__(kPackThreads, 3)
     pack_searched_kernel(const __nv_bfloat16* __restrict__ W, const float* __restrict__ s,
                          const float* __restrict__ qp, const int32_t* __restrict__ best_idx, int G, int64_t D_in,
                          int64_t D_out, uint8_t* __restrict__ qweight, __half* __restrict__ scales,
                          __half* __restrict__ zeros) {
-  constexpr int RB = GS / kPackRows;  // row blocks per group
   const int64_t chunks = D_out / kQChunkCols;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * kPackThreads + threadIdx.x;
+  if (c >= chunks) return;
   const int64_t T = D_in / GS;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * kPackThreads + threadIdx.x;
-  if (idx >= T * RB * chunks) return;
-  const int64_t c = idx % chunks;
-  const int64_t rest = idx / chunks;
-  const int rb = static_cast<int>(rest % RB);
-  const int64_t g = rest / RB;
   const int64_t n = c * kQChunkCols;
-  const int64_t row0 = g * GS + rb * kPackRows;
+  int k = *best_idx;
+  k = k < 0 ? 0 : (k >= G ? G - 1 : k);  // awq_search always writes an index in [0, G)
+  for (int64_t rbg = blockIdx.y; rbg < D_in / kPackRows; rbg += gridDim.y) {
+  const int64_t row0 = rbg * kPackRows;
+  const int64_t g = row0 / GS;
+  const bool first_block = (row0 % GS) == 0;
 
   uint4 w[kPackRows];
 #pragma unroll
@@ -420,9 +424,7 @@ __global__ void __launch_bounds__(kPackThreads, 3)
     sj[i + 2] = v.z;
     sj[i + 3] = v.w;
   }
-  // {1/step x8, 1.5*2^23 + zero x8, step x8} of (best candidate, group, chunk)
-  int k = *best_idx;
-  k = k < 0 ? 0 : (k >= G ? G - 1 : k);  // awq_search always writes an index in [0, G)
+  // {1/step x8, 1.5*2^23 + zero x8, step x8, clamp flag, ...} of (best candidate, group, chunk)
   const float* qc = qp + ((static_cast<int64_t>(k) * T + g) * chunks + c) * kQChunkFloats;
   const float4* q4 = reinterpret_cast<const float4*>(qc);
   float inv[8], zmz[8];  // zmz: 1.5*2^23 + the stored offset (the zero; 8 for symmetric codes)
@@ -441,7 +443,7 @@ __global__ void __launch_bounds__(kPackThreads, 3)
       for (int j = 0; j < 8; ++j) zmz[j] = za[j];
     }
   }
-  if (rb == 0) {
+  if (first_block) {
     const float4 s0 = q4[4], s1 = q4[5];
     const float st[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
     uint32_t sc[4], zr[4];
@@ -456,20 +458,25 @@ __global__ void __launch_bounds__(kPackThreads, 3)
     *reinterpret_cast<uint4*>(zeros + g * D_out + n) = make_uint4(zr[0], zr[1], zr[2], zr[3]);
   }
   uint32_t out[kPackRows / 2][2];
-  if (codes_8x8<SYM>(w, sj, inv, zmz, out) > kTieGuard || has_zero15<SYM>(zmz)) {
+  // the table's clamp flag, for the same codes the search formed; one path per warp
+  const bool clampw = __any_sync(__activemask(), qc[kQChunkClamp] != 0.f);
+  const float tmax = clampw ? codes_8x8<SYM, true>(w, sj, inv, zmz, out) : codes_8x8<SYM, false>(w, sj, inv, zmz, out);
+  if (tmax > kTieGuard || has_zero15<SYM>(zmz)) {
     pack_exact_8x8<SYM>(W, s, qc, row0, n, D_out, qweight);
-    return;
+  } else {
+    store_codes_8x8(out, row0, n, D_out, qweight);
   }
-  store_codes_8x8(out, row0, n, D_out, qweight);
+  }
 }
 
 template <int GS, bool SYM>
 cudaError_t launch_pack_searched_t(const void* W, const float* s, const float* qp, const int32_t* best_idx, int G,
                                    int64_t D_in, int64_t D_out, uint8_t* qweight, void* scales, void* zeros,
                                    cudaStream_t stream) {
-  const int64_t threads = (D_in / GS) * (GS / kPackRows) * (D_out / kQChunkCols);
-  const int64_t blocks = (threads + kPackThreads - 1) / kPackThreads;
-  pack_searched_kernel<GS, SYM><<<static_cast<unsigned>(blocks), kPackThreads, 0, stream>>>(
+  const int64_t xblocks = (D_out / kQChunkCols + kPackThreads - 1) / kPackThreads;
+  const int64_t yblocks = std::min<int64_t>(D_in / kPackRows, 65535);
+  const dim3 grid(static_cast<unsigned>(xblocks), static_cast<unsigned>(yblocks));
+  pack_searched_kernel<GS, SYM><<<grid, kPackThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(W), s, qp, best_idx, G, D_in, D_out, qweight, static_cast<__half*>(scales),
       static_cast<__half*>(zeros));
   return cudaGetLastError();

@@ -248,19 +248,36 @@ __global__ void __launch_bounds__(kGpThreads, 7) group_params_kernel(const __nv_
     }
   }
   if (bad && blockIdx.z == 0) set_error(status, AWQ_DEV_NONFINITE);
-  if (n >= D_out) return;
+  // every thread of the warp takes part in the chunk flags' ballot below
+  const bool valid = n < D_out;
   const int64_t T = D_in / GS;
   const int64_t kstride = T * (D_out / kQChunkCols) * kQChunkFloats;
   float* dst0 = qp + k0 * kstride + (grp * (D_out / kQChunkCols) + n / kQChunkCols) * kQChunkFloats +
                 (n % kQChunkCols);
+  const int lane = t & 31;
+  // the code range with the table's offset: zm = 1.5*2^23 + zero, and zero 0
+  // for symmetric codes (stored +8 only by the pack)
+  const float qlo = symmetric ? kMagic - 7.f : kMagic, qhi = symmetric ? kMagic + 7.f : kMagic + 15.f;
 #pragma unroll
   for (int k = 0; k < kMaxGpCandidates; ++k) {
     if (k < nk) {
       const QParam q = make_qparam(lo[k], hi[k], symmetric, status);
-      float* dst = dst0 + k * kstride;
-      dst[0] = q.inv;
-      dst[kQChunkCols] = q.zm;
-      dst[2 * kQChunkCols] = q.step;
+      // The codes of a column leave the code range only at its extremes:
+      // rint is monotone, so the column's largest code is the one of the
+      // range's top, fma(hi, 1/step, 1.5*2^23 + zero), and its smallest the
+      // one of the range's bottom, formed with the same fused multiply-add
+      // and rounding as the searches' and the pack's codes.  A non-finite
+      // range fails both comparisons.
+      const float bottom = symmetric ? -hi[k] : lo[k];
+      const bool need = valid && !(__fmaf_rn(hi[k], q.inv, q.zm) <= qhi && __fmaf_rn(bottom, q.inv, q.zm) >= qlo);
+      const uint32_t chunk_bits = (__ballot_sync(0xFFFFFFFFu, need) >> (lane & ~(kQChunkCols - 1))) & 0xFFu;
+      if (valid) {
+        float* dst = dst0 + k * kstride;
+        dst[0] = q.inv;
+        dst[kQChunkCols] = q.zm;
+        dst[2 * kQChunkCols] = q.step;
+        if ((n % kQChunkCols) == 0) dst[3 * kQChunkCols] = chunk_bits ? 1.f : 0.f;
+      }
     }
   }
 }

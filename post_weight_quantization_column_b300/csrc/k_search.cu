@@ -107,10 +107,13 @@ __device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
 // Four rows x 8 columns of the negated difference tile D = W - S^-1 W'hat:
 //   w' = w s;  t = rint(w' / step) + zero, held as 1.5*2^23 + code;  clamp
 //   to the code range;  d = (w' - (code - zero) step) / s.
-// (D and -D give the same loss.)  `w` points at the 16-byte chunk of row 0
+// (D and -D give the same loss.)  CLAMP = false leaves out the clamps, for
+// warps none of whose columns has a code outside the range in this group
+// (the group-parameter table's per-chunk flag).  `w` points at the 16-byte chunk of row 0
 // in the swizzled B slot; row i's chunk sits at w + i*128 with its 16-byte
 // position XOR-ed by i (rows 4*half .. 4*half+3 of an 8-row swizzle atom).
 // Each chunk of W is overwritten in place by the same chunk of D.
+template <bool CLAMP>
 __device__ __forceinline__ void produce4(uint8_t* w, int c8, int half, float4 s4, float4 r4,
                                          const float2 (&inv2)[4], const float2 (&zm2)[4],
                                          const float2 (&nzm2)[4], const float2 (&nstep2)[4], float lo, float hi) {
@@ -131,8 +134,10 @@ __device__ __forceinline__ void produce4(uint8_t* w, int c8, int half, float4 s4
       const float2 w2 = make_float2(bf16lo(wu[j]), bf16hi(wu[j]));
       const float2 wp = __fmul2_rn(w2, s2);
       float2 tq = __ffma2_rn(wp, inv2[j], zm2[j]);
-      tq.x = fminf(fmaxf(tq.x, lo), hi);
-      tq.y = fminf(fmaxf(tq.y, lo), hi);
+      if (CLAMP) {
+        tq.x = fminf(fmaxf(tq.x, lo), hi);
+        tq.y = fminf(fmaxf(tq.y, lo), hi);
+      }
       const float2 qz = __fadd2_rn(tq, nzm2[j]);
       const float2 ev = __ffma2_rn(qz, nstep2[j], wp);
       const float2 d = __fmul2_rn(ev, r2);
@@ -367,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     for (int t = pair; t < p.num_tiles && !*abort_flag; t += npairs) {
       int cached_group = -1;
+      bool clampw = true;
       float2 inv2[4], zm2[4], nzm2[4], nstep2[4];
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -380,9 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int grp = (kb * kBK) / p.group_size;
         if (grp != cached_group) {
           cached_group = grp;
-          // chunk c: {1/step x8, 1.5*2^23 + zero x8, step x8, unused x4}
+          // chunk c: {1/step x8, 1.5*2^23 + zero x8, step x8, clamp flag, unused x3}
           const float4* qp = reinterpret_cast<const float4*>(side + 2 * kSBytes + c * (kQChunkFloats * 4));
           const float4 i0 = qp[0], i1 = qp[1], z0 = qp[2], z1 = qp[3], s0 = qp[4], s1 = qp[5];
+          // one path per warp: the clamps stay unless no column of the warp needs them
+          clampw = __any_sync(0xFFFFFFFFu, qp[6].x != 0.f);
           inv2[0] = make_float2(i0.x, i0.y);
           inv2[1] = make_float2(i0.z, i0.w);
           inv2[2] = make_float2(i1.x, i1.y);
@@ -401,10 +409,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* srow = reinterpret_cast<const float*>(side) + rg * 8;
         const float* rrow = reinterpret_cast<const float*>(side + kSBytes) + rg * 8;
         uint8_t* wrow = smem + kOffB + s * kBBytes + h * (kBK * 128) + (rg * 8) * 128;
+        if (clampw) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half)
-          produce4(wrow + half * 4 * 128, c8, half, *reinterpret_cast<const float4*>(srow + half * 4),
-                   *reinterpret_cast<const float4*>(rrow + half * 4), inv2, zm2, nzm2, nstep2, lo, hi);
+          for (int half = 0; half < 2; ++half)
+            produce4<true>(wrow + half * 4 * 128, c8, half, *reinterpret_cast<const float4*>(srow + half * 4),
+                           *reinterpret_cast<const float4*>(rrow + half * 4), inv2, zm2, nzm2, nstep2, lo, hi);
+        } else {
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+            produce4<false>(wrow + half * 4 * 128, c8, half, *reinterpret_cast<const float4*>(srow + half * 4),
+                            *reinterpret_cast<const float4*>(rrow + half * 4), inv2, zm2, nzm2, nstep2, lo, hi);
+        }
         fence_proxy_async_smem();  // stores visible to the tensor cores
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(bfull0 + static_cast<uint32_t>(s) * 8u);
