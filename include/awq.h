@@ -210,6 +210,37 @@ AWQ_API awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D
                       void* ws, size_t ws_bytes, awq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The search sharded over output columns (several processes, one GPU each).
+ * "AWQ (Activation-aware Weight Quantization)", 缩放因子优化的完整流程 step 4c:
+ * L is a squared Frobenius norm, a sum over output columns, so the candidates'
+ * losses of the whole layer are the sums of the losses of disjoint column
+ * slices.  Each rank runs awq_search on X and its slice W[:, c0:c1], copies
+ * out the search's block partials, the ranks gather them in slice order, and
+ * each rank selects the global alpha* from all of them; the searched pack of
+ * each slice then uses that alpha*.
+ *
+ * awq_search_block_losses: after awq_search(N, D_in, D_out, G, cfg, ws), its
+ *   fp64 block partials: blk [G, nb], nb = ceil(D_out / 256); blk[k][b] is
+ *   the candidate-k loss of columns [256 b, 256 b + 256), summed in the
+ *   search's fixed order.  Device to device copy, asynchronous on `stream`.
+ * awq_search_select: blk holds [G, nb] block partials of all slices, each
+ *   slice's blocks in column order and the slices in order (nb the total);
+ *   writes losses [G] (the blocks summed in order, fp64), best_idx (first
+ *   smallest loss) and s_star [D_in] (s of that candidate, from the scale
+ *   table in ws), into the caller's buffers.  ws, N, D_in, D_out, G, cfg: this
+ *   rank's own awq_search call; pass that call's losses, best_idx and s_star
+ *   to overwrite them, so that awq_quantize_pack_searched on ws packs this
+ *   rank's slice at the global alpha*.  When every slice but the last spans a
+ *   multiple of 256 columns, the losses equal those of one awq_search of the
+ *   whole layer bit for bit.  All losses NaN: AWQ_ERR_NONFINITE in ws.
+ * ------------------------------------------------------------------------- */
+AWQ_API awq_status awq_search_block_losses(const void* ws, size_t ws_bytes, int64_t N, int64_t D_in, int64_t D_out,
+                                           int32_t G, const awq_cfg* cfg, double* blk, awq_stream_t stream);
+AWQ_API awq_status awq_search_select(const double* blk, int64_t nb, int32_t G, void* ws, size_t ws_bytes,
+                                     int64_t N, int64_t D_in, int64_t D_out, const awq_cfg* cfg, double* losses,
+                                     int32_t* best_idx, float* s_star, awq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Step 4: offline quantisation and nibble packing of diag(s) W.
  * "AWQ (Activation-aware Weight Quantization)", 推理时的等效实现:
  * W_quantized = Quantize(diag(s*) W); "009. AWQ Integration", Consequences:

@@ -76,7 +76,12 @@ _SIGS = {
     "awq_w4a16_workspace_size": ([_c_i64, _c_i64, _c_i64, ctypes.POINTER(_c_sz)], ctypes.c_int),
     "awq_w4a16_matmul": ([_vp, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp, ctypes.POINTER(awq_cfg), _vp, _vp, _c_sz,
                           _vp], ctypes.c_int),
+    "awq_search_block_losses": ([_vp, _c_sz, _c_i64, _c_i64, _c_i64, _c_i32, ctypes.POINTER(awq_cfg), _vp, _vp],
+                                ctypes.c_int),
+    "awq_search_select": ([_vp, _c_i64, _c_i32, _vp, _c_sz, _c_i64, _c_i64, _c_i64, ctypes.POINTER(awq_cfg), _vp,
+                          _vp, _vp, _vp], ctypes.c_int),
     "awq_selftest_gemm_bf16": ([_vp, _vp, _c_i32, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_sz, _vp], ctypes.c_int),
+    "awq_selftest_wait_timeout": ([ctypes.c_uint64, _c_i32, _vp, _vp, _c_sz, _vp], ctypes.c_int),
     "awq_profile_enable": ([_c_i32], ctypes.c_int),
     "awq_profile_collect": ([ctypes.POINTER(awq_kernel_time), _c_i32, ctypes.POINTER(_c_i32)], ctypes.c_int),
 }
@@ -221,6 +226,10 @@ class SearchResult:
     col_losses: Optional[torch.Tensor]  # fp64 [G, D_out] or None
     grid: list
     workspace: torch.Tensor
+    # the call that filled it (set by search(); used by the column-sharded form)
+    shape: tuple = ()           # (N, D_in, D_out)
+    cfg: tuple = ()             # (group_size, symmetric, act_floor)
+    gram: bool = False
 
     @property
     def best(self) -> int:
@@ -282,7 +291,42 @@ def search(X: torch.Tensor, W: torch.Tensor, mean_abs: torch.Tensor, grid=None, 
               _stream_handle(stream)), name)
     if check:
         check_workspace(ws, f"{name} (device)", stream)
+    out.workspace, out.shape, out.cfg, out.gram = ws, (N, D_in, D_out), (group_size, symmetric, act_floor), gram
     return out
+
+
+def search_block_losses(res: SearchResult, stream=None) -> torch.Tensor:
+    """The fp64 block partials [G, ceil(D_out / 256)] of a finished search
+    (each the candidate's loss over 256 consecutive output columns)."""
+    if res.gram or len(res.shape) != 3:
+        raise ValueError("block partials are available from a direct search() result")
+    N, D_in, D_out = res.shape
+    G = len(res.grid)
+    cfg = make_cfg(res.cfg[0], res.cfg[1], 4, res.cfg[2])
+    blk = torch.empty(G, (D_out + 255) // 256, dtype=torch.float64, device=res.workspace.device)
+    _check(lib().awq_search_block_losses(_ptr(res.workspace), res.workspace.numel(), N, D_in, D_out, G,
+                                         ctypes.byref(cfg), _ptr(blk), _stream_handle(stream)),
+           "awq_search_block_losses")
+    return blk
+
+
+def search_select(res: SearchResult, blk: torch.Tensor, stream=None, check: bool = True) -> SearchResult:
+    """Overwrite res.losses / best_idx / s_star from block partials [G, nb] of
+    all column slices (slice order): the global alpha* of a column-sharded
+    search, written where awq_quantize_pack_searched reads it."""
+    _need(blk, torch.float64, "blk")
+    N, D_in, D_out = res.shape
+    G = len(res.grid)
+    if blk.dim() != 2 or blk.shape[0] != G:
+        raise ValueError("blk must be [G, nb]")
+    blk = blk.contiguous()
+    cfg = make_cfg(res.cfg[0], res.cfg[1], 4, res.cfg[2])
+    _check(lib().awq_search_select(_ptr(blk), blk.shape[1], G, _ptr(res.workspace), res.workspace.numel(), N, D_in,
+                                   D_out, ctypes.byref(cfg), _ptr(res.losses), _ptr(res.best_idx), _ptr(res.s_star),
+                                   _stream_handle(stream)), "awq_search_select")
+    if check:
+        check_workspace(res.workspace, "awq_search_select (device)", stream)
+    return res
 
 
 # ---------------------------------------------------------------------- step 4
@@ -429,6 +473,17 @@ def selftest_gemm(A: torch.Tensor, B: torch.Tensor, b_mn_major: bool = True, str
                                         ws.numel(), _stream_handle(stream)), "awq_selftest_gemm_bf16")
     check_workspace(ws, "awq_selftest_gemm_bf16 (device)", stream)
     return C
+
+
+def selftest_wait_timeout(limit_ns: int, pairs: int, ws: torch.Tensor, stream=None) -> list:
+    """Run the CTA-pair kernels' abort path on waits that never complete
+    (test helper).  Returns the kernel's record [CTAs finished, CTAs whose
+    wait expired, longest CTA run time in microseconds, CTAs whose bulk copy
+    landed intact]; the status word of ws is left at AWQ_ERR_TIMEOUT."""
+    record = torch.zeros(4, dtype=torch.int32, device=ws.device)
+    _check(lib().awq_selftest_wait_timeout(int(limit_ns), int(pairs), _ptr(record), _ptr(ws), ws.numel(),
+                                           _stream_handle(stream)), "awq_selftest_wait_timeout")
+    return [int(v) for v in record.cpu().tolist()]
 
 
 # ---------------------------------------------------------------------- profiling aid

@@ -416,6 +416,40 @@ awq_status awq_search(const void* X, const void* W, int64_t N, int64_t D_in, int
                     encode, s);
 }
 
+awq_status awq_search_block_losses(const void* ws, size_t ws_bytes, int64_t N, int64_t D_in, int64_t D_out,
+                                  int32_t G, const awq_cfg* cfg, double* blk, awq_stream_t stream) {
+  awq_status st = validate_search_shape(N, D_in, D_out, G, cfg);
+  if (st != AWQ_OK) return st;
+  if (!ws || !blk) return AWQ_ERR_INVALID_ARG;
+  if (!aligned(ws, 256) || !aligned(blk, 8)) return AWQ_ERR_ALIGNMENT;
+  const SearchLayout L = search_layout(N, D_in, D_out, G, cfg->group_size);
+  if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
+  st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  const size_t bytes = static_cast<size_t>(G) * static_cast<size_t>(reduce_blocks(D_out)) * sizeof(double);
+  return from_cuda(cudaMemcpyAsync(blk, static_cast<const uint8_t*>(ws) + L.blk, bytes, cudaMemcpyDeviceToDevice,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+awq_status awq_search_select(const double* blk, int64_t nb, int32_t G, void* ws, size_t ws_bytes, int64_t N,
+                             int64_t D_in, int64_t D_out, const awq_cfg* cfg, double* losses, int32_t* best_idx,
+                             float* s_star, awq_stream_t stream) {
+  awq_status st = validate_search_shape(N, D_in, D_out, G, cfg);
+  if (st != AWQ_OK) return st;
+  if (nb < 1 || nb > (int64_t(1) << 40)) return AWQ_ERR_SHAPE;
+  if (!blk || !ws || !losses || !best_idx || !s_star) return AWQ_ERR_INVALID_ARG;
+  if (!aligned(blk, 8) || !aligned(ws, 256) || !aligned(losses, 8) || !aligned(best_idx, 4) || !aligned(s_star, 4))
+    return AWQ_ERR_ALIGNMENT;
+  const SearchLayout L = search_layout(N, D_in, D_out, G, cfg->group_size);
+  if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
+  st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const float* s_tab = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + L.s_tab);
+  ProfScope prof("select", cs);
+  return from_cuda(launch_select_losses(blk, nb, G, losses, best_idx, s_tab, D_in, s_star, status_word(ws), cs));
+}
+
 awq_status awq_search_gram_workspace_size(int64_t N, int64_t D_in, int64_t D_out, int32_t G, const awq_cfg* cfg,
                                           size_t* bytes) {
   if (!bytes) return AWQ_ERR_INVALID_ARG;
@@ -681,6 +715,22 @@ awq_status awq_selftest_gemm_bf16(const void* A, const void* B, int32_t b_mn_maj
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return AWQ_ERR_CUDA;
   return from_cuda(launch_gemm_store(encode, A, B, b_mn_major, M, N, K, C, status_word(ws), cs));
+}
+
+awq_status awq_selftest_wait_timeout(uint64_t limit_ns, int32_t pairs, uint32_t* record, void* ws, size_t ws_bytes,
+                                     awq_stream_t stream) {
+  if (!record || !ws) return AWQ_ERR_INVALID_ARG;
+  if (limit_ns < 1000 || limit_ns > 2000ull * 1000ull * 1000ull) return AWQ_ERR_INVALID_ARG;
+  if (pairs < 1 || pairs > 1024) return AWQ_ERR_SHAPE;
+  if (!aligned(ws, 256) || !aligned(record, 4)) return AWQ_ERR_ALIGNMENT;
+  if (ws_bytes < kHeaderBytes + 4096) return AWQ_ERR_WORKSPACE;
+  awq_status st = check_device(nullptr);
+  if (st != AWQ_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), cs) != cudaSuccess) return AWQ_ERR_CUDA;
+  if (cudaMemsetAsync(record, 0, 4 * sizeof(uint32_t), cs) != cudaSuccess) return AWQ_ERR_CUDA;
+  return from_cuda(launch_abort_selftest(static_cast<uint8_t*>(ws) + kHeaderBytes, limit_ns, pairs, status_word(ws),
+                                         record, cs));
 }
 
 // ------------------------------------------------------------------ profiling

@@ -84,6 +84,12 @@ constexpr int kGemmBK = 64;
 cudaError_t launch_gemm_store(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* A, const void* B, int b_mn_major,
                               int64_t M, int64_t N, int64_t K, float* C, uint32_t* status, cudaStream_t stream);
 
+// Test-only: `pairs` CTA pairs run the abort protocol of the pair kernels on
+// mbarriers that never complete, with waits bounded by limit_ns (src: 4 KB of
+// device memory, 16-byte aligned, copied into each CTA; record: uint32 [4]).
+cudaError_t launch_abort_selftest(const void* src, uint64_t limit_ns, int pairs, uint32_t* status, uint32_t* record,
+                                  cudaStream_t stream);
+
 // ----------------------------------------------------------------- fused search (CTA pairs)
 // Rows of X per partial-sum slot of the fused search: [G][m_tiles][D_out].
 int search_fused_m_tiles(int64_t N);
@@ -121,6 +127,11 @@ cudaError_t launch_search_fused(PFN_cuTensorMapEncodeTiled_v12000 encode, const 
 
 // ----------------------------------------------------------------- reductions
 int reduce_blocks(int64_t D_out);
+constexpr int kReduceBlockCols = 256;  // columns summed by one block partial
+// L_k = the blocks of blk [G][nb] summed in order, first argmin, s* = s_k*.
+cudaError_t launch_select_losses(const double* blk, int64_t nb, int G, double* losses, int32_t* best_idx,
+                                 const float* s_tab, int64_t D_in, float* s_star, uint32_t* status,
+                                 cudaStream_t stream);
 // blk: fp64 [G][reduce_blocks(D_out)] scratch; ticket: a zeroed uint32 (left zeroed).
 cudaError_t launch_reduce_losses(const float* partial, int m_tiles, int64_t D_out, int G, double* col_losses,
                                  double* blk, unsigned int* ticket, double* losses, int32_t* best_idx,

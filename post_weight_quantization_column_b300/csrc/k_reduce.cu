@@ -97,6 +97,55 @@ __global__ void __launch_bounds__(kRedThreads)
   }
 }
 
+// The final step of the reduction over block partials gathered from several
+// searches of disjoint column slices (each slice's blocks in column order,
+// the slices in order): L_k = sum over blocks in order, the first argmin, and
+// s* = s_k* from this search's scale table.  With slices that start on
+// 256-column boundaries the blocks are the ones one search of the whole
+// layer forms, and the sums are the same to the last bit.
+__global__ void __launch_bounds__(kRedThreads)
+    select_losses_kernel(const double* __restrict__ blk, int64_t nb, int G, double* __restrict__ losses,
+                         int32_t* __restrict__ best_idx, const float* __restrict__ s_tab, int64_t D_in,
+                         float* __restrict__ s_star, uint32_t* status) {
+  __shared__ double sh[kMaxGrid];
+  __shared__ int kbest;
+  if (threadIdx.x < G) {
+    double L = 0.0;
+    for (int64_t b = 0; b < nb; ++b) L += blk[static_cast<int64_t>(threadIdx.x) * nb + b];
+    sh[threadIdx.x] = L;
+    losses[threadIdx.x] = L;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int b = -1;
+    double bl = 0.0;
+    for (int kk = 0; kk < G; ++kk) {
+      const double L = sh[kk];
+      if (isnan(L)) continue;
+      if (b < 0 || L < bl) {
+        b = kk;
+        bl = L;
+      }
+    }
+    if (b < 0) {
+      b = 0;
+      set_error(status, AWQ_DEV_NONFINITE);
+    }
+    kbest = b;
+    *best_idx = b;
+  }
+  __syncthreads();
+  const float* src = s_tab + static_cast<int64_t>(kbest) * D_in;
+  for (int64_t j = threadIdx.x; j < D_in; j += kRedThreads) s_star[j] = src[j];
+}
+
+cudaError_t launch_select_losses(const double* blk, int64_t nb, int G, double* losses, int32_t* best_idx,
+                                 const float* s_tab, int64_t D_in, float* s_star, uint32_t* status,
+                                 cudaStream_t stream) {
+  select_losses_kernel<<<1, kRedThreads, 0, stream>>>(blk, nb, G, losses, best_idx, s_tab, D_in, s_star, status);
+  return cudaGetLastError();
+}
+
 int reduce_blocks(int64_t D_out) { return static_cast<int>((D_out + kRedThreads - 1) / kRedThreads); }
 
 cudaError_t launch_reduce_losses(const float* partial, int m_tiles, int64_t D_out, int G, double* col_losses,

@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bempty_bar[kBStages];  // both CTAs: MMAs done with the B slot
   __shared__ __align__(8) uint64_t acc_full_bar;
   __shared__ __align__(8) uint64_t acc_empty_bar;
+  __shared__ __align__(8) uint64_t mma_drain_bar;          // even CTA: MMAs still running after an abort
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&acc_full_bar, 1);
     mbar_init(&acc_empty_bar, kAccEmptyCount);
+    mbar_init(&mma_drain_bar, 1);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -175,6 +177,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int first = it - kAStages < 0 ? 0 : it - kAStages;
       for (int j = first; j < it; ++j)
         mbar_wait_cluster(&aempty_bar[j % kAStages], (j / kAStages) & 1, p.status, abort_flag);
+      if (*abort_flag) {
+        // after an abort those waits return at once: the X copies still in
+        // flight land first.  Their completion is counted on the even CTA's
+        // barriers, so the even CTA waits there (bounded: a phase the peer
+        // never filled cannot complete) and the odd CTA gives them the same time.
+        if (leader)
+          for (int j = first; j < it; ++j)
+            mbar_wait_cluster(&afull_bar[j % kAStages], (j / kAStages) & 1, nullptr, nullptr, kCopyDrainNs);
+        else
+          settle_ns(kCopyDrainNs);
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer (even CTA)
@@ -212,6 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit_pair_mc(&acc_full_bar, 0x3);
       }
       if (tc > 0 && !*abort_flag) mbar_wait_cluster(&acc_empty_bar, (tc - 1) & 1, p.status, abort_flag);
+      if (*abort_flag) {
+        // no MMA of the pair may still run when TMEM is freed: one more
+        // commit arrives once every MMA issued so far is done
+        umma_commit_pair_mc(&mma_drain_bar, 0x1);
+        mbar_wait(&mma_drain_bar, 0, nullptr, nullptr, kCopyDrainNs);
+      }
     }
   } else if (warp == 2) {
     // ---------------------------------------------------------- code / side-input loader
@@ -238,6 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int first = it - kBStages < 0 ? 0 : it - kBStages;
       for (int j = first; j < it; ++j)
         mbar_wait_cluster(&bempty_bar[j % kBStages], (j / kBStages) & 1, p.status, abort_flag);
+      if (*abort_flag)  // after an abort: this CTA's own copies in flight land first
+        for (int j = first; j < it; ++j)
+          mbar_wait(&cfull_bar[j % kBStages], (j / kBStages) & 1, nullptr, nullptr, kCopyDrainNs);
     }
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
     // ---------------------------------------------------------- epilogue

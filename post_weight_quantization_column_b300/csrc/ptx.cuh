@@ -59,15 +59,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // role of the CTA leaves its loop.  Returns true when the phase completed;
 // false on a timeout or when another role raised *abort.
 constexpr uint64_t kWaitLimitNs = 2000ull * 1000ull * 1000ull;  // 2 s
+// Bound of the waits for copies still in flight after an abort: a copy lands
+// within microseconds, unless its phase can no longer complete.
+constexpr uint64_t kCopyDrainNs = 1000ull * 1000ull;  // 1 ms
 constexpr uint32_t kWaitMaxPolls = 1u << 30;
 
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_wait_impl(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                               volatile int* abort_flag);
+                                               volatile int* abort_flag, uint64_t limit_ns = kWaitLimitNs);
 
+// limit_ns: the wall-time bound of this wait (the product kernels keep the
+// default; a self-test passes a short one to make a wait expire).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                          volatile int* abort_flag) {
-  return mbar_wait_impl<false>(bar, parity, status, abort_flag);
+                                          volatile int* abort_flag, uint64_t limit_ns = kWaitLimitNs) {
+  return mbar_wait_impl<false>(bar, parity, status, abort_flag, limit_ns);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -214,14 +219,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_wait_impl(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                               volatile int* abort_flag) {
+                                               volatile int* abort_flag, uint64_t limit_ns) {
   auto poll = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1; i < kWaitMaxPolls; ++i) {
     if (poll()) return true;
     if (abort_flag && *abort_flag) return false;
-    if ((i & 15u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+    if ((i & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) break;
   }
   set_error(status, AWQ_DEV_TIMEOUT);
   if (abort_flag) *abort_flag = 1;
@@ -231,8 +236,13 @@ __device__ __forceinline__ bool mbar_wait_impl(uint64_t* bar, uint32_t parity, u
 // Bounded wait with cluster-scope acquire (the phase may complete through
 // arrivals from the peer CTA).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                                  volatile int* abort_flag) {
-  return mbar_wait_impl<true>(bar, parity, status, abort_flag);
+                                                  volatile int* abort_flag, uint64_t limit_ns = kWaitLimitNs) {
+  return mbar_wait_impl<true>(bar, parity, status, abort_flag, limit_ns);
+}
+// Sleep for about `ns` of wall time (copies in flight land meanwhile).
+__device__ __forceinline__ void settle_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) __nanosleep(10000);
 }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");

@@ -150,3 +150,16 @@ def test_calls_validate_before_cuda(L):
     assert mm(fake, 0, 256, 256, fake, fake, fake, None, ctypes.byref(cfg), fake, fake, 256, None) == 0
     # self-test GEMM: K not a multiple of 64
     assert L.awq_selftest_gemm_bf16(fake, fake, 1, 128, 256, 100, fake, fake, 256, None) == 2
+
+
+def test_wait_timeout_selftest_validates_on_host(L):
+    f = L.awq_selftest_wait_timeout
+    f.argtypes = [ctypes.c_uint64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    fake = ctypes.c_void_p(0x100000)
+    assert f(999, 1, fake, fake, 8192, None) == 1                  # limit below 1 us
+    assert f(2_000_000_001, 1, fake, fake, 8192, None) == 1        # limit above the product's 2 s
+    assert f(1_000_000, 0, fake, fake, 8192, None) == 2            # no pair
+    assert f(1_000_000, 1, fake, ctypes.c_void_p(0x100010), 8192, None) == 3  # ws not 256-byte aligned
+    assert f(1_000_000, 1, fake, fake, 4096, None) == 4            # no room for the 4 KB copy source
+    assert f(1_000_000, 1, None, fake, 8192, None) == 1
