@@ -1,8 +1,8 @@
 // Loss reduction and argmin ("AWQ (Activation-aware Weight Quantization)",
 // 缩放因子优化的完整流程 steps 4c-6): the search leaves one fp32 sum of squares
-// per (candidate, row tile, column); these are summed in fp64 in a fixed
-// order, first over row tiles (per-column losses), then over columns (L_k),
-// then k* = first argmin and s* = s_k* is copied out.
+// per (candidate, row tile, column); these are summed in a fixed order, first
+// over row tiles (per-column losses), then over columns (L_k, fp64), then
+// k* = first argmin and s* = s_k* is copied out.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -12,8 +12,11 @@ constexpr int kRedThreads = 256;
 
 // One kernel for the whole reduction.  CTA (bx, k) owns columns
 // [256 bx, 256 bx + 256) of candidate k: each thread sums its column over the
-// row tiles (fp64, tile order) into col[k][n]; the CTA then sums its 256
-// columns in a fixed tree into blk[k][bx].  The last CTA to finish (a ticket
+// row tiles into col[k][n] -- each run of 8 tiles as a fixed fp32 pairwise
+// tree (error below 3 * 2^-24 of the run's sum of squares), the runs in tile
+// order in fp64, which keeps fp64 adds (slow on this part) to one per 8
+// tiles; the CTA then sums its 256 columns in a fixed fp64 tree into
+// blk[k][bx].  The last CTA to finish (a ticket
 // counter that the caller zeroed) adds blk[k][0..nb) in block order into
 // L_k, picks k* = first argmin and copies s* = s_k*.  Every sum has a fixed
 // order, so the result does not depend on timing.
@@ -31,15 +34,13 @@ __global__ void __launch_bounds__(kRedThreads)
   double v = 0.0;
   if (n < D_out) {
     const float* p = partial + static_cast<int64_t>(k) * m_tiles * D_out + n;
-    int m = 0;
-    for (; m + 8 <= m_tiles; m += 8) {
-      float x[8];  // eight loads in flight, added in tile order
+    for (int m = 0; m < m_tiles; m += 8) {
+      float x[8];  // eight loads in flight; tiles past the end count as 0
 #pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = p[static_cast<int64_t>(m + i) * D_out];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v += static_cast<double>(x[i]);
+      for (int i = 0; i < 8; ++i) x[i] = m + i < m_tiles ? p[static_cast<int64_t>(m + i) * D_out] : 0.f;
+      const float t = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+      v += static_cast<double>(t);
     }
-    for (; m < m_tiles; ++m) v += static_cast<double>(p[static_cast<int64_t>(m) * D_out]);
     col[static_cast<int64_t>(k) * D_out + n] = v;
   }
   sh[threadIdx.x] = v;
