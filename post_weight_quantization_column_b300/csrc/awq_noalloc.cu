@@ -13,8 +13,8 @@ namespace {
 // Layout of the array: a 256-byte header (status word at word 0) | one ticket
 // counter per 256-channel chunk | 4 MiB of fp32 row-slice partial sums.  Every
 // device that loads the library holds it until the process exits.  The row-
-// slice plan of the statistic uses at most max(1, 444 / chunks) slices, so
-// splits * D_in <= max(D_in, 444 * 256) floats: every D_in up to
+// slice plan of the statistic uses at most max(1, 296 / chunks) slices, so
+// splits * D_in <= max(D_in, 296 * 256) floats: every D_in up to
 // kNoAllocScratchFloats fits.
 constexpr int64_t kNoAllocScratchFloats = int64_t(1) << 20;
 constexpr int64_t kNoAllocHeaderWords = 64;

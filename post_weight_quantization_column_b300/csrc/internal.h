@@ -14,9 +14,9 @@ namespace awqdev {
 constexpr int kStatsRowLanes = 8;      // consumer warps per CTA, each on its own rows of a box
 constexpr int kStatsThreads = (kStatsRowLanes + 1) * 32;  // + one producer warp
 constexpr int kStatsCols = 256;        // channels per CTA (32 lanes x 8)
-constexpr int kStatsBoxRows = 32;      // rows per ring stage (one bulk copy per row)
-constexpr int kStatsStages = 4;        // ring depth: 4 x 16 KB
-constexpr int kStatsTargetCtas = 148 * 3;  // three CTAs (3 x 73 KB shared memory) fit on an SM
+constexpr int kStatsBoxRows = 32;      // rows per ring stage (one tensor copy per box)
+constexpr int kStatsStages = 6;        // ring depth: 6 x 16 KB
+constexpr int kStatsTargetCtas = 148 * 2;  // two CTAs (2 x 105 KB shared memory) on each SM
 constexpr int kStatsMaxSplits = 1024;
 
 void stats_plan(int64_t N, int64_t D, int* splits, int64_t* rows_per_split);

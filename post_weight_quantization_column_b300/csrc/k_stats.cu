@@ -3,14 +3,14 @@
 // aiqz.cc article "awq-activation-aware-quantization", section 1 (I_i = E|X_i|).
 //
 // HBM-bound column reduction.  A CTA owns 256 consecutive channels and one
-// slice of rows.  Its producer thread streams the slice through a 4-stage
+// slice of rows.  Its producer thread streams the slice through a 6-stage
 // ring of 32-row x 256-channel boxes (one 16 KB tensor copy each), so a CTA
-// keeps 64 KB of X in flight with one instruction per box and the loads do
-// not depend on the SM's issue rate.  Eight consumer warps take interleaved
+// keeps 96 KB of X in flight with one instruction per box and the loads do
+// not depend on the SM's issue rate; two CTAs share an SM.  Eight consumer warps take interleaved
 // rows of each box: lane l adds the 8 channels 8l .. 8l+7.  Rows past N and
 // channels past D arrive as zeros.  Per-thread sums are fp32, the 8 warps are combined in
-// a fixed order through shared memory, and the row slices are summed in fp64
-// in slice order by the last CTA of each column chunk to finish (a per-chunk
+// a fixed order through shared memory, and the row slices are summed in a
+// fixed fp32 tree by the last CTA of each column chunk to finish (a per-chunk
 // ticket counter), so the result does not depend on timing.
 #include <cuda_bf16.h>
 
@@ -193,23 +193,27 @@ __global__ void __launch_bounds__(kStatsThreads) act_stats_kernel(const __grid_c
   // a slice that timed out set the status word before its ticket
   const bool poison = nan_on_error && status && *reinterpret_cast<volatile uint32_t*>(status) != 0u;
   if (t < kStatsCols && t < width) {
-    // the slices in order, 32 loads in flight per batch (one batch unless
-    // the grid has more than 32 slices)
+    // the slices in batches of 32 (one batch unless the grid has more than
+    // 32 slices), each batch as a fixed pairwise tree in fp32, the batches in
+    // order: the error stays below (5 + batches) * 2^-24 of the total, and
+    // no fp64 arithmetic (slow on this part) sits on the kernel's tail
     const int splits = static_cast<int>(gridDim.y);
-    double s = 0.0;
+    float s = 0.f;
     for (int k = 0; k < splits; k += 32) {
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = k + i < splits ? partial[static_cast<int64_t>(k + i) * D + j] : 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (k + i < splits) s += static_cast<double>(v[i]);
+      for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) v[i] += v[i + w];
+      s += v[0];
     }
     if (!isfinite(s)) set_error(status, AWQ_DEV_NONFINITE);
     if (sum_abs) {
-      sum_abs[j] += s;  // this CTA alone owns channel j now
+      sum_abs[j] += static_cast<double>(s);  // this CTA alone owns channel j now
     } else {
-      mean_abs[j] = poison ? __int_as_float(0x7FC00000) : static_cast<float>(s / static_cast<double>(N));
+      mean_abs[j] = poison ? __int_as_float(0x7FC00000) : __fdiv_rn(s, static_cast<float>(N));
     }
     if (kMax) {
       float m = max_abs[j];

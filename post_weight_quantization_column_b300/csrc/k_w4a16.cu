@@ -508,8 +508,8 @@ cudaError_t launch_w4a16(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X
 //   sum_j x'_j (q_j - z) sc = sc (sum_j x'_j q_j - z sum_j x'_j),
 // so a weight costs a nibble unpack and one FMA per row of X.  The 8 warps'
 // sums are added in warp order, the CTA's partial goes to the workspace, and
-// the last CTA of a column block (ticket) adds the row blocks in order (fp64)
-// and writes Y in bf16.
+// the last CTA of a column block (ticket) adds the row blocks in a fixed
+// order (fp32 pairwise trees of 16, then in order) and writes Y in bf16.
 namespace {
 
 constexpr int kDecCols = 256;       // columns per CTA (32 lanes x 8)
@@ -642,16 +642,21 @@ __global__ void __launch_bounds__(kDecThreads)
   for (int i = t; i < MT * kDecCols; i += kDecThreads) {
     const int m = i / kDecCols, c = i % kDecCols;
     if (m < M && n0 + c < D_out) {
-      double v = 0.0;
+      // 16 row blocks' loads in flight, each batch as a fixed pairwise fp32
+      // tree, the batches in order (fp64 adds are slow on this part)
+      float v = 0.f;
       for (int64_t b0 = 0; b0 < rb_count; b0 += 16) {
-        float pv[16];  // 16 row blocks' loads in flight, added in block order
+        float pv[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           pv[k] = b0 + k < rb_count ? partial[((b0 + k) * M + m) * D_out + n0 + c] : 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) v += static_cast<double>(pv[k]);
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int k = 0; k < w; ++k) pv[k] += pv[k + w];
+        v += pv[0];
       }
-      Y[static_cast<int64_t>(m) * D_out + n0 + c] = __float2bfloat16_rn(static_cast<float>(v));
+      Y[static_cast<int64_t>(m) * D_out + n0 + c] = __float2bfloat16_rn(v);
     }
   }
   if (t == 0) tickets[blockIdx.x] = 0u;  // ready for the next call
