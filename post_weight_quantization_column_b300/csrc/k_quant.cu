@@ -31,23 +31,51 @@ __device__ __forceinline__ bool bf16x2_nonfinite(uint32_t u) {
 // ------------------------------------------------------------------ scales
 // s_kj = fp32(pow(fp64(max(a_j, floor)), alpha_k)), r_kj = 1/s_kj (IEEE).
 // "AWQ (Activation-aware Weight Quantization)", 缩放因子优化的完整流程 step 3.
-__global__ void scale_table_kernel(const float* __restrict__ mean_abs, int64_t D, AlphaGrid grid, float act_floor,
-                                   float* __restrict__ s_tab, float* __restrict__ r_tab, uint32_t* status) {
+//
+// fp64 arithmetic is slow on this part, and pow is the costliest of it.  A
+// thread owns one channel j and up to kScaleCands candidates: log2(a_j)
+// once, then per candidate y = exp2(alpha_k log2 a_j), both in fp64.  With the CUDA math
+// library's documented maximum errors (1 ulp for log2 and for exp2) and
+// |log2 a| <= 150 for any positive fp32 a, y is within (1.04 * 150 + 1) *
+// 2^-52 relative of a^alpha, i.e. within 320 fp64 ulps.  Unless y lies within
+// 2^10 ulps of a point where fp32 rounding changes (half-way between two fp32
+// values), fp32(y) is fp32 of the exact power and of pow's result; near such
+// a point the thread takes pow itself, so the table is what pow gives.
+__device__ __forceinline__ float fp32_power(double a, double la, double alpha) {
+  const double y = exp2(alpha * la);
+  // bits below fp32 precision: 29 of the 52-bit fraction; the rounding point
+  // is 1 followed by zeros there
+  const long long bits = __double_as_longlong(y);
+  const long long low = bits & ((1ll << 29) - 1);
+  const long long dist = low >= (1ll << 28) ? low - (1ll << 28) : (1ll << 28) - low;
+  const bool normal = y >= 1.1754943508222875e-38 && y <= 3.4028234663852886e38;  // fp32 normal range
+  if (!normal || dist <= (1ll << 10)) return static_cast<float>(pow(a, alpha));
+  return static_cast<float>(y);
+}
+
+constexpr int kScaleCands = 4;  // candidates per thread: blockIdx.y takes the next four
+
+__global__ void scale_table_kernel(const float* __restrict__ mean_abs, int64_t D, AlphaGrid grid, int G,
+                                   float act_floor, float* __restrict__ s_tab, float* __restrict__ r_tab,
+                                   uint32_t* status) {
   const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int k = blockIdx.y;
   if (j >= D) return;
   const float a = mean_abs[j];
-  if (!isfinite(a) && k == 0) set_error(status, AWQ_DEV_NONFINITE);
-  const float af = fmaxf(a, act_floor);
-  const float s = static_cast<float>(pow(static_cast<double>(af), grid.a[k]));
-  s_tab[static_cast<int64_t>(k) * D + j] = s;
-  r_tab[static_cast<int64_t>(k) * D + j] = __fdiv_rn(1.0f, s);
+  if (!isfinite(a) && blockIdx.y == 0) set_error(status, AWQ_DEV_NONFINITE);
+  const double af = static_cast<double>(fmaxf(a, act_floor));
+  const double la = log2(af);
+  const int k1 = min(G, static_cast<int>(blockIdx.y + 1) * kScaleCands);
+  for (int k = blockIdx.y * kScaleCands; k < k1; ++k) {
+    const float s = isfinite(la) ? fp32_power(af, la, grid.a[k]) : static_cast<float>(pow(af, grid.a[k]));
+    s_tab[static_cast<int64_t>(k) * D + j] = s;
+    r_tab[static_cast<int64_t>(k) * D + j] = __fdiv_rn(1.0f, s);
+  }
 }
 
 cudaError_t launch_scale_table(const float* mean_abs, int64_t D_in, const AlphaGrid& grid, int G, float act_floor,
                                float* s_tab, float* r_tab, uint32_t* status, cudaStream_t stream) {
-  const dim3 g(static_cast<unsigned>((D_in + 255) / 256), static_cast<unsigned>(G));
-  scale_table_kernel<<<g, 256, 0, stream>>>(mean_abs, D_in, grid, act_floor, s_tab, r_tab, status);
+  const dim3 g(static_cast<unsigned>((D_in + 127) / 128), static_cast<unsigned>((G + kScaleCands - 1) / kScaleCands));
+  scale_table_kernel<<<g, 128, 0, stream>>>(mean_abs, D_in, grid, G, act_floor, s_tab, r_tab, status);
   return cudaGetLastError();
 }
 

@@ -71,6 +71,8 @@ constexpr int kGroupWarps = 4;                   // producer warps per K step (t
 static_assert(kProdWarps == 2 * kGroupWarps, "two producer groups");
 constexpr int kBFullCount = 2 * kGroupWarps;     // one producer group of each CTA
 constexpr int kAccEmptyCount = 2 * kEpiWarps;
+constexpr int kHeadSteps = 3;                    // K steps a tile starts on subtile 0 alone
+static_assert(kHeadSteps <= kAStages && kHeadSteps <= kBStages, "the held head steps fit in both rings");
 
 static_assert(kSmemBytes + 1024 + 4608 <= 227 * 1024, "shared memory (dynamic + alignment slack + static)");
 
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bfull_bar[kBStages];   // even CTA: D written by both CTAs
   __shared__ __align__(8) uint64_t bempty_bar[kBStages];  // both CTAs: MMAs done with the B slot
   __shared__ __align__(8) uint64_t acc_full_bar;          // both CTAs
-  __shared__ __align__(8) uint64_t acc_empty_bar;         // even CTA
+  __shared__ __align__(8) uint64_t acc_empty_bar[kStack];  // even CTA: subtile s of the accumulator read out
   __shared__ __align__(8) uint64_t mma_drain_bar;          // even CTA: MMAs still running after an abort
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bempty_bar[s], 1);
     }
     mbar_init(&acc_full_bar, 1);
-    mbar_init(&acc_empty_bar, kAccEmptyCount);
+    for (int sub = 0; sub < kStack; ++sub) mbar_init(&acc_empty_bar[sub], kAccEmptyCount);
     mbar_init(&mma_drain_bar, 1);
     abort_sh = 0;
     fence_mbar_init();
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // shared::cluster addresses of the even CTA's barriers
   const uint32_t afull0 = mapa_shared(smem_u32(&afull_bar[0]), 0);
   const uint32_t bfull0 = mapa_shared(smem_u32(&bfull_bar[0]), 0);
-  const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty_bar), 0);
+  const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty_bar[0]), 0);
 
   if (warp == 0) {
     // ---------------------------------------------------------- X loader
@@ -267,40 +269,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       // M = 256 (pair), N = 256, bf16 x bf16 -> fp32, A K-major, B N-major
       constexpr uint32_t idesc = idesc_bf16_f32(256, kPairN, 0, 1);
       int it = 0, tc = 0;
+      // Issue the MMAs of K step `it` for subtiles [sub0, sub1) of the accumulator.
+      auto issue = [&](int it_, int kb, int sub0, int sub1) {
+        const int sa = it_ % kAStages;
+        const int sb = it_ % kBStages;
+        const uint32_t a_addr = smem_u32(smem + sa * kABytes);
+        const uint32_t b_addr = smem_u32(smem + kOffB + sb * kBBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // B: N-major SW128; 64-column chunks 8 KB apart (LBO), 8-row K
+          // groups 1024 B apart (SBO); a K step of 16 is two K groups.
+          const uint64_t bd = sdesc_sw128(b_addr + kk * 2048, kBK * 128, 1024);
+          for (int sub = sub0; sub < sub1; ++sub) {
+            const uint64_t ad = sdesc_sw128(a_addr + sub * kASubBytes + kk * 32, 16, 1024);
+            umma_bf16_pair(tmem + static_cast<uint32_t>(sub * kPairN), ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+        }
+      };
+      auto inputs_ready = [&](int it_) {
+        return mbar_wait_cluster(&afull_bar[it_ % kAStages], (it_ / kAStages) & 1, p.status, abort_flag) &&
+               mbar_wait_cluster(&bfull_bar[it_ % kBStages], (it_ / kBStages) & 1, p.status, abort_flag);
+      };
+      auto release = [&](int it_) {
+        umma_commit_pair_mc(&aempty_bar[it_ % kAStages], 0x3);
+        umma_commit_pair_mc(&bempty_bar[it_ % kBStages], 0x3);
+      };
       for (int t = pair; t < p.num_tiles; t += npairs, ++tc) {
-        if (tc > 0 && !mbar_wait_cluster(&acc_empty_bar, (tc - 1) & 1, p.status, abort_flag)) break;
+        // The epilogue reads the previous tile's subtile 0 first and releases
+        // it on its own barrier: the first kHeadSteps K steps of this tile
+        // start on subtile 0 (holding their stages) while subtile 1 is still
+        // being read out, which hides part of the drain between tiles.
+        if (tc > 0 && !mbar_wait_cluster(&acc_empty_bar[0], (tc - 1) & 1, p.status, abort_flag)) break;
         tc_fence_after();
+        const int head = KB < kHeadSteps ? KB : kHeadSteps;
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int sa = it % kAStages;
-          const int sb = it % kBStages;
-          if (!mbar_wait_cluster(&afull_bar[sa], (it / kAStages) & 1, p.status, abort_flag) ||
-              !mbar_wait_cluster(&bfull_bar[sb], (it / kBStages) & 1, p.status, abort_flag)) {
+        for (int kb = 0; kb < head; ++kb) {
+          if (!inputs_ready(it + kb)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + sa * kABytes);
-          const uint32_t b_addr = smem_u32(smem + kOffB + sb * kBBytes);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // B: N-major SW128; 64-column chunks 8 KB apart (LBO), 8-row K
-            // groups 1024 B apart (SBO); a K step of 16 is two K groups.
-            const uint64_t bd = sdesc_sw128(b_addr + kk * 2048, kBK * 128, 1024);
-#pragma unroll
-            for (int sub = 0; sub < kStack; ++sub) {
-              const uint64_t ad = sdesc_sw128(a_addr + sub * kASubBytes + kk * 32, 16, 1024);
-              umma_bf16_pair(tmem + static_cast<uint32_t>(sub * kPairN), ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-            }
+          issue(it + kb, kb, 0, 1);
+        }
+        if (!ok) break;
+        if (tc > 0 && !mbar_wait_cluster(&acc_empty_bar[1], (tc - 1) & 1, p.status, abort_flag)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < head; ++kb) {
+          issue(it + kb, kb, 1, kStack);
+          release(it + kb);
+        }
+        it += head;
+        for (int kb = head; kb < KB; ++kb, ++it) {
+          if (!inputs_ready(it)) {
+            ok = false;
+            break;
           }
-          umma_commit_pair_mc(&aempty_bar[sa], 0x3);
-          umma_commit_pair_mc(&bempty_bar[sb], 0x3);
+          tc_fence_after();
+          issue(it, kb, 0, kStack);
+          release(it);
         }
         if (!ok) break;
         umma_commit_pair_mc(&acc_full_bar, 0x3);
       }
       // the epilogues' last arrivals (some remote) land before the pair exits
-      if (tc > 0 && !*abort_flag) mbar_wait_cluster(&acc_empty_bar, (tc - 1) & 1, p.status, abort_flag);
+      if (tc > 0 && !*abort_flag)
+        for (int sub = 0; sub < kStack; ++sub)
+          mbar_wait_cluster(&acc_empty_bar[sub], (tc - 1) & 1, p.status, abort_flag);
       if (*abort_flag) {
         // no MMA of the pair may still run when TMEM is freed: one more
         // commit arrives once every MMA issued so far is done
@@ -349,25 +383,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tc = 0;
     for (int t = pair; t < p.num_tiles; t += npairs, ++tc) {
       const Tile tl = decode_tile(t, p);
-      bool ok = mbar_wait(&acc_full_bar, tc & 1, p.status, abort_flag);
+      // one warp polls the accumulator barrier; the other seven sleep in a
+      // hardware barrier until it has seen the phase (no polling traffic for
+      // the length of a tile), and all learn whether the wait succeeded
+      bool ok = true;
+      if (e == 0) ok = mbar_wait(&acc_full_bar, tc & 1, p.status, abort_flag);
+      ok = !named_bar_or(2, kEpiWarps * 32, !ok);
       tc_fence_after();
       if (ok) {
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        // subtile 0, then subtile 1, each released as soon as this warp has
+        // read it: per column, the sum of squares of each subtile's 128 rows
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int col = ch * 128 + cc * 32;
-          float a[32], b[32];
-          tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(col), a);
-          tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kPairN + col), b);
-          if (cc == 3) {
-            // every TMEM read of this warp is complete: release the accumulator
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(acc_empty0);
-          }
+        for (int sub = 0; sub < kStack; ++sub) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            const int col = ch * 128 + cc * 32;
+            float a[32];
+            tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(sub * kPairN + col), a);
+            if (cc == 3) {
+              // every TMEM read of this subtile by this warp is complete
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_remote(acc_empty0 + static_cast<uint32_t>(sub) * 8u);
+            }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) a[i] = fmaf(a[i], a[i], b[i] * b[i]);
-          red[q][col + lane] = transpose_sum32(a, lane);
+            for (int i = 0; i < 32; ++i) a[i] = a[i] * a[i];
+            const float v = transpose_sum32(a, lane);
+            if (sub == 0)
+              red[q][col + lane] = v;
+            else
+              red[q][col + lane] += v;
+          }
         }
       }
       if (named_bar_or(1, kEpiWarps * 32, !ok || *abort_flag)) break;
