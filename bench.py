@@ -44,6 +44,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="large_mlp")
     ap.add_argument("--extras", default="all",
                     help="measurements after the step: all, none, or a comma list of pack_any,w4a16,gram,greedy")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="calibration rows instead of the workload's (reduced profiler captures); 0 = the workload's")
     ap.add_argument("--grid", type=int, default=21)
     ap.add_argument("--flush-mib", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -293,12 +295,19 @@ def cpu_model():
 
 
 # ---------------------------------------------------------------------------- reference arm
+def workload_of(args):
+    import dataclasses
+
+    from post_weight_quantization_column_b300 import synth
+    w = synth.WORKLOADS[args.workload]
+    return dataclasses.replace(w, N=args.rows) if args.rows > 0 else w
+
+
 def run_reference(args, world, rank):
     from post_weight_quantization_column_b300 import synth
-    import numpy as np
     if rank != 0:
         return 0
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     X, W = synth.generate(w)
     Xf, Wf = synth.bf16_to_f32(X), synth.bf16_to_f32(W)
     from oracle import awq_oracle as orc
@@ -440,7 +449,6 @@ def measure_greedy(awq, Wd, a_buf, g, sym, flush_l2, world):
 
 # ---------------------------------------------------------------------------- our arm
 def run_ours(args, world, rank, local):
-    import numpy as np
     import torch
 
     import post_weight_quantization_column_b300 as awq
@@ -449,7 +457,7 @@ def run_ours(args, world, rank, local):
     if not os.path.exists(awq.LIB_PATH):
         raise SystemExit("libawq_b300.so is not built: run `python -m post_weight_quantization_column_b300.build`")
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     G = args.grid
     grid = awq.default_grid(G)
     X, W = synth.generate(w)

@@ -40,6 +40,9 @@
 // AWQ_ERR_TIMEOUT and every role leaves its loop.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <cmath>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -79,6 +82,7 @@ static_assert(kSmemBytes + 1024 + 4608 <= 227 * 1024, "shared memory (dynamic + 
 struct FusedArgs {
   int N, D_in, D_out, G, T, group_size;
   int m_blocks, n_blocks, num_tiles, m_tiles;
+  int sb_m, sb_n;  // super-block: sb_m row bands x sb_n column blocks (see decode_tile)
   float clamp_lo, clamp_hi;
   float* partial;  // [G][m_tiles][D_out]
   uint32_t* status;
@@ -152,12 +156,24 @@ __device__ __forceinline__ void produce4(uint8_t* w, int c8, int half, float4 s4
 struct Tile {
   int k, m_blk, n_blk;
 };
+// Work units in an L2-sized order: candidate fastest, then the units of one
+// super-block of sb_m row bands x sb_n column blocks (column block fastest),
+// super-blocks column-major within a strip of sb_m bands, strips in order.
+// A super-block's X rows, W columns and parameter rows stay in L2 while all
+// candidates of all its units run, so W and the parameter table come from
+// HBM once per strip instead of once per row band.
 __device__ __forceinline__ Tile decode_tile(int t, const FusedArgs& p) {
   Tile r;
   r.k = t % p.G;
-  const int rest = t / p.G;
-  r.n_blk = rest % p.n_blocks;
-  r.m_blk = rest / p.n_blocks;
+  const int u = t / p.G;
+  const int strip = u / (p.sb_m * p.n_blocks);  // every earlier strip is full
+  const int in_strip = u - strip * (p.sb_m * p.n_blocks);
+  const int mb = min(p.sb_m, p.m_blocks - strip * p.sb_m);  // bands in this strip
+  const int sbk = in_strip / (mb * p.sb_n);                 // every earlier super-block of the strip is full
+  const int in_sb = in_strip - sbk * (mb * p.sb_n);
+  const int nb = min(p.sb_n, p.n_blocks - sbk * p.sb_n);    // column blocks in this super-block
+  r.m_blk = strip * p.sb_m + in_sb / nb;
+  r.n_blk = sbk * p.sb_n + in_sb % nb;
   return r;
 }
 
@@ -578,6 +594,15 @@ cudaError_t launch_search_fused(PFN_cuTensorMapEncodeTiled_v12000 encode, const 
   a.n_blocks = static_cast<int>((D_out + kPairN - 1) / kPairN);
   a.num_tiles = G * a.m_blocks * a.n_blocks;
   a.m_tiles = 2 * a.m_blocks;
+  {
+    // super-blocks: about 32 MB of X rows and 48 MB of W columns with their
+    // parameter rows, together well inside the 126 MB L2
+    const double x_band = 2.0 * kStack * kSubRows * 2.0 * static_cast<double>(D_in);
+    const double w_blk = static_cast<double>(D_in) * kPairN * 2.0 +
+                         static_cast<double>(G) * T * (kPairN / kQChunkCols) * kQChunkFloats * 4.0;
+    a.sb_m = static_cast<int>(std::min<double>(a.m_blocks, std::max(1.0, std::floor(32e6 / x_band))));
+    a.sb_n = static_cast<int>(std::min<double>(a.n_blocks, std::max(1.0, std::floor(48e6 / w_blk))));
+  }
   constexpr float kMagic = 12582912.0f;
   a.clamp_lo = symmetric ? kMagic - 7.f : kMagic;
   a.clamp_hi = symmetric ? kMagic + 7.f : kMagic + 15.f;
