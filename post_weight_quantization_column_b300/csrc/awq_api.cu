@@ -640,11 +640,13 @@ awq_status awq_greedy_search(const void* W, const float* mean_abs, int64_t D_in,
 
 // ------------------------------------------------------------------ W4A16 product
 namespace {
-// W4A16 workspace: header | (decode path) tickets [D_out/256] | partials [D_in/256][M][D_out]
+// W4A16 workspace: header | (decode path) tickets [D_out/1024] | B fragments of x' [D_in/64 chunks] |
+// partials [1024 + D_out/1024][M][1024]
 size_t w4a16_ticket_bytes(int64_t D_out) { return align_up(static_cast<size_t>(w4a16_decode_tickets(D_out)) * 4, 256); }
+size_t w4a16_xprep_bytes(int64_t D_in) { return align_up(static_cast<size_t>(w4a16_decode_xprep_bytes(D_in)), 256); }
 size_t w4a16_ws_bytes(int64_t M, int64_t D_in, int64_t D_out) {
   if (M > kW4a16DecodeMaxRows) return kHeaderBytes;
-  return kHeaderBytes + w4a16_ticket_bytes(D_out) +
+  return kHeaderBytes + w4a16_ticket_bytes(D_out) + w4a16_xprep_bytes(D_in) +
          align_up(static_cast<size_t>(w4a16_decode_partial_floats(M, D_in, D_out)) * 4, 256);
 }
 }  // namespace
@@ -673,20 +675,21 @@ awq_status awq_w4a16_matmul(const void* X, int64_t M, int64_t D_in, int64_t D_ou
   int dev = 0;
   st = check_device(&dev);
   if (st != AWQ_OK) return st;
-  if (M <= kW4a16DecodeMaxRows) {
-    // a few rows: the CUDA-core path that reads the codes once
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const size_t tb = w4a16_ticket_bytes(D_out);
-    if (cudaMemsetAsync(ws, 0, kHeaderBytes + tb, cs) != cudaSuccess) return AWQ_ERR_CUDA;
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    ProfScope prof("w4a16_decode", cs);
-    return from_cuda(launch_w4a16_decode(X, M, D_in, D_out, qweight, scales, zeros, s, cfg->group_size, Y,
-                                         reinterpret_cast<float*>(base + kHeaderBytes + tb),
-                                         reinterpret_cast<unsigned int*>(base + kHeaderBytes), cs));
-  }
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   st = get_encode(&encode);
   if (st != AWQ_OK) return st;
+  if (M <= kW4a16DecodeMaxRows) {
+    // a few rows: the CUDA-core path that reads the codes once
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const size_t tb = w4a16_ticket_bytes(D_out), xb = w4a16_xprep_bytes(D_in);
+    // the header and the tickets are zeroed by the path's first kernel
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    ProfScope prof("w4a16_decode", cs);
+    return from_cuda(launch_w4a16_decode(encode, X, M, D_in, D_out, qweight, scales, zeros, s, cfg->group_size, Y,
+                                         reinterpret_cast<float*>(base + kHeaderBytes + tb + xb),
+                                         reinterpret_cast<unsigned int*>(base + kHeaderBytes),
+                                         base + kHeaderBytes + tb, status_word(ws), cs));
+  }
   int pairs = 0;
   st = get_w4a16_pairs(dev, &pairs);
   if (st != AWQ_OK) return st;

@@ -95,13 +95,16 @@ cudaError_t launch_abort_selftest(const void* src, uint64_t limit_ns, int pairs,
 int search_fused_m_tiles(int64_t N);
 // CTA pairs that fit on the device at once (occupancy query).
 cudaError_t search_fused_max_pairs(int* pairs);
-// Decode-sized W4A16 product (M <= kW4a16DecodeMaxRows) on CUDA cores.
+// Decode-sized W4A16 product (M <= kW4a16DecodeMaxRows): the B fragments of
+// x' = x / s into xf [xprep bytes], then a persistent register-fed MMA kernel.
 constexpr int64_t kW4a16DecodeMaxRows = 4;
 int64_t w4a16_decode_partial_floats(int64_t M, int64_t D_in, int64_t D_out);
 int64_t w4a16_decode_tickets(int64_t D_out);
-cudaError_t launch_w4a16_decode(const void* X, int64_t M, int64_t D_in, int64_t D_out, const uint8_t* qweight,
-                                const void* scales, const void* zeros, const float* s, int group_size, void* Y,
-                                float* partial, unsigned int* tickets, cudaStream_t stream);
+int64_t w4a16_decode_xprep_bytes(int64_t D_in);
+cudaError_t launch_w4a16_decode(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, int64_t M, int64_t D_in,
+                                int64_t D_out, const uint8_t* qweight, const void* scales, const void* zeros,
+                                const float* s, int group_size, void* Y, float* partial, unsigned int* tickets,
+                                uint8_t* xf, uint32_t* status, cudaStream_t stream);
 // The Gram form of the search: X^T (zero past N, row length ldt), the
 // blocked fp32 Cholesky of H in place (lower; Linv: a 64 x 64 fp32 scratch
 // block), R = L^T in bf16.

@@ -26,6 +26,9 @@
 // Every mbarrier wait is bounded; a timeout records AWQ_ERR_TIMEOUT and every
 // role leaves its loop.
 #include <cuda_bf16.h>
+
+#include <algorithm>
+#include <atomic>
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -499,195 +502,490 @@ cudaError_t launch_w4a16(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X
 }
 
 // ---------------------------------------------------------------------------
-// Decode-sized W4A16 product (M <= 4 rows of X): the codes are read once and
-// the work is a handful of FMAs per weight, so CUDA cores keep up with HBM.
-// A CTA owns 256 columns x 256 input rows; warp w takes rows 32w .. 32w+31
-// (inside one group for every group size), lane l columns 8l .. 8l+7, one
-// 8-byte code load per byte row.  x' = x / s of the CTA's rows sits in shared
-// memory.  Per group the dequantisation is factored out of the sum:
-//   sum_j x'_j (q_j - z) sc = sc (sum_j x'_j q_j - z sum_j x'_j),
-// so a weight costs a nibble unpack and one FMA per row of X.  The 8 warps'
-// sums are added in warp order, the CTA's partial goes to the workspace, and
-// the last CTA of a column block (ticket) adds the row blocks in a fixed
-// order (fp32 pairwise trees of 16, then in order) and writes Y in bf16.
+// Decode-sized W4A16 product (M <= 4 rows of X).  A few rows of X make the
+// product a stream over the codes: every code byte is read once and used for
+// M rows, so the kernel must turn 4-bit codes into products at HBM speed.  It
+// does so on the tensor cores through register-fed mma.sync (m16n8k16, bf16
+// in, fp32 accumulate), which keeps the codes in registers: a tcgen05 tile
+// (M >= 64) would be mostly padding here and would force the unpacked
+// weights through shared memory.
+//
+// Unpacking.  A 32-bit word of one byte row holds the codes of 4 columns
+// c .. c+3 for input rows 2j (low nibbles) and 2j+1 (high nibbles).  One
+// masked OR (w >> 4s) & 0x000F000F | 0x43004300 turns it into the bf16 pair
+// (128 + q[row][c + s'], 128 + q[row][c + s' + 2]) -- 128 + q is exact in
+// bf16 -- so 8 codes cost 3 shifts and 4 logic operations.  The pair holds
+// two columns of one row, so the MMA's reduction index runs over
+// (row, parity e in {0, 1}) with column c + 2e, and B carries x' in the slot
+// of its own parity and zero in the other:
+//   A (16 x 16): row g <-> column base c_g (rows g + 8: c_g + 1),
+//                k = 2t + e <-> (input row of k pair t, column offset 2e);
+//   B (16 x 8):  n = 4e' + 2m + h <-> (parity e', row m of X, x'_hi or
+//                x'_lo), with x'_hi = bf16(x'), x'_lo = bf16(x' - x'_hi) of
+//                x' = x / s, so the bf16 products lose nothing beyond 2^-16
+//                of x'; B[(row, e)][n] = x'_h[row][m] if e = e' else 0;
+//   D (16 x 8):  D[g][n] = sum over the rows of (128 + q[row][c_g + 2e'])
+//                x'_h[row][m].
+// Per group, with xs = sum of x'_hi + x'_lo over the group's rows (fp32,
+// fixed order): y += sc (D_hi + D_lo - (z + 128) xs) = sc sum_j x'_j (q_j - z)
+// ("AWQ (Activation-aware Weight Quantization)", 量化数学基础 step 3:
+// Dequant = (q - z) s).  Rows 2 and 3 of X take a second n tile.
+//
+// A stage is 64 input rows x 1024 columns (32 KB of code bytes, eight
+// 128-column tensor copies with the 128-byte swizzle) plus the rows' B
+// fragments and row sums (xprep_kernel writes them once per call) and the
+// group row of fp16 scales and zeros.  Consumer warp w owns columns
+// 64w .. 64w+63; a k group is the 4 byte rows 8b + 2t + par (t = 0..3) of
+// one parity in a block b of 8, so the 8-byte loads of a warp meet no bank
+// conflicts under the swizzle; lane (g, t) = (lane / 4, lane % 4) loads
+// columns 8g .. 8g+7 of byte row 8b + 2t + par, two words for two MMA tiles.
+// Stages are taken in column-block-major order; persistent CTAs own equal
+// contiguous runs of stages.  Where a run leaves a column block the CTA's
+// sums go to slot (CTA + column block) of the workspace (the pair grows
+// along every run, so slots never collide); the last CTA to finish a column
+// block (a ticket counter per block) adds its segments top to bottom as
+// fixed fp32 pairwise trees of 8 and writes Y in bf16.
 namespace {
 
-constexpr int kDecCols = 256;       // columns per CTA (32 lanes x 8)
-constexpr int kDecRows = 256;       // input rows per CTA (8 warps x 32)
-constexpr int kDecThreads = 256;
+constexpr int kDqCols = 1024;                              // columns per stage
+constexpr int kDqBoxCols = 128;                            // per tensor copy (128-byte swizzle)
+constexpr int kDqWarpCols = 64;                            // per consumer warp
+constexpr int kDqRows = 64;                                // input rows per stage
+constexpr int kDqByteRows = kDqRows / 2;
+constexpr int kDqKGroups = kDqByteRows / 4;                // 8 k groups of 4 byte rows
+constexpr int kDqConsumers = kDqCols / kDqWarpCols;        // 16
+constexpr int kDqThreads = (kDqConsumers + 1) * 32;
+constexpr int kDqStages = 5;
+constexpr int kDqCtasPerSm = 1;
+constexpr int kDqNTiles = 2;                               // n tiles: rows 0-1 and 2-3 of X
+constexpr int kDqCodeBytes = kDqByteRows * kDqCols;        // 32 KB
+constexpr int kDqBoxBytes = kDqByteRows * kDqBoxCols;      // 4 KB, 1024-byte aligned
+constexpr int kDqFragBytes = kDqKGroups * kDqNTiles * 32 * 8;  // B fragments of 64 rows
+constexpr int kDqChunkBytes = kDqFragBytes + 16;           // + xs of the 64 rows for 4 rows of X
+constexpr int kDqSideBytes = kDqCols * 2;                  // one group row of fp16
+constexpr int kDqSideBox = 256;                            // fp16 columns per side copy
+constexpr int kDqOffFrag = kDqCodeBytes;
+constexpr int kDqOffSc = (kDqOffFrag + kDqChunkBytes + 127) / 128 * 128;
+constexpr int kDqOffZ = kDqOffSc + kDqSideBytes;
+constexpr int kDqStageTx = kDqCodeBytes + kDqChunkBytes + 2 * kDqSideBytes;
+constexpr int kDqStageStride = (kDqOffZ + kDqSideBytes + 1023) / 1024 * 1024;
+constexpr int kDqSmem = kDqStages * kDqStageStride + 1024;  // + alignment slack
+constexpr int64_t kDqMaxCtas = 1024;                       // bound of the grid (workspace sizing)
+constexpr uint32_t kDqBias = 0x43004300u;                  // bf16 pair (128, 128)
+static_assert(kDqSmem <= 227 * 1024 && kDqCtasPerSm * (kDqSmem + 1024) <= 228 * 1024, "shared memory per SM");
+static_assert(kDqChunkBytes % 16 == 0 && kDqOffSc % 128 == 0 && kDqOffZ % 128 == 0, "copy alignment");
 
-template <int MT>
-__global__ void __launch_bounds__(kDecThreads)
-    w4a16_decode_kernel(const __nv_bfloat16* __restrict__ X, int M, int64_t D_in, int64_t D_out,
-                        const uint8_t* __restrict__ qweight, const __half* __restrict__ scales,
-                        const __half* __restrict__ zeros, const float* __restrict__ s, int group_size,
-                        float* __restrict__ partial, unsigned int* __restrict__ tickets, __nv_bfloat16* __restrict__ Y) {
-  __shared__ float xs[MT][kDecRows];                  // x' = x / s of the CTA's rows
-  __shared__ float red[kDecThreads / 64][MT][kDecCols];  // warps w and w + 4 add into slot w
-  __shared__ bool last;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kDecCols;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kDecRows;
-  const int rows = static_cast<int>(min(static_cast<int64_t>(kDecRows), D_in - r0));  // a multiple of 64
-  for (int i = t; i < MT * kDecRows; i += kDecThreads) {
-    const int m = i / kDecRows, r = i % kDecRows;
-    float v = 0.f;
-    if (m < M && r < rows) {
-      v = __bfloat162float(X[static_cast<int64_t>(m) * D_in + r0 + r]);
-      if (s) v = __fdiv_rn(v, s[r0 + r]);
+__device__ __forceinline__ void bulk_g2s_dq(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// (x & 0x000F000F) | bias in one logic operation (bias kept in a register).
+__device__ __forceinline__ uint32_t code_pair(uint32_t x, uint32_t bias) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(d) : "r"(x), "r"(bias));
+  return d;
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint2 lds_u32x2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(__nv_bfloat16 h) { return *reinterpret_cast<const uint16_t*>(&h); }
+
+// x' = x / s (x when s is null), zero for rows of X past M.
+__device__ __forceinline__ float xprime(const __nv_bfloat16* X, int M, int64_t D_in, const float* s, int m,
+                                        int64_t row) {
+  if (m >= M) return 0.f;
+  const float v = __bfloat162float(X[static_cast<int64_t>(m) * D_in + row]);
+  return s ? __fdiv_rn(v, s[row]) : v;
+}
+__device__ __forceinline__ void split_hi_lo(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+// One CTA per 64-row chunk: the B fragments of its 8 k groups and 2 n tiles
+// in the order the MMA reads them, and, per row of X, xs = sum of x'_hi +
+// x'_lo over the 64 rows in row order.  CTA 0 also zeroes the workspace
+// header (status word) and the ticket counters of the product that follows,
+// which may start before this grid ends (programmatic dependent launch) and
+// reads none of this before it waits for it.
+constexpr int kXprepThreads = 4 * kDqRows;
+__global__ void __launch_bounds__(kXprepThreads) xprep_kernel(const __nv_bfloat16* __restrict__ X, int M,
+                                                              int64_t D_in, const float* __restrict__ s,
+                                                              uint8_t* __restrict__ xf, uint32_t* __restrict__ header,
+                                                              unsigned int* __restrict__ tickets, int64_t ntickets) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t ch = blockIdx.x;
+  uint8_t* dst = xf + ch * kDqChunkBytes;
+  const int tid = threadIdx.x, lane = tid & 31, kg = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int e = g >> 2, h = g & 1;
+  const int blk = kg >> 1, par = kg & 1;
+  const int64_t r_lo = ch * kDqRows + 16 * blk + 4 * t + 2 * par;  // byte row 8 blk + 2t + par, low nibble
+  if (ch == 0) {
+    if (tid < 64) header[tid] = 0u;
+    for (int64_t i = tid; i < ntickets; i += kXprepThreads) tickets[i] = 0u;
+  }
+#pragma unroll
+  for (int nt = 0; nt < kDqNTiles; ++nt) {
+    const int m = 2 * nt + ((g >> 1) & 1);
+    uint32_t b[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      __nv_bfloat16 hi, lo;
+      split_hi_lo(xprime(X, M, D_in, s, m, r_lo + q), hi, lo);
+      const uint32_t v = bf16_bits(h ? lo : hi);
+      b[q] = e ? (v << 16) : v;  // the slot of parity e; the other parity's slot is zero
     }
-    xs[m][r] = v;
+    reinterpret_cast<uint2*>(dst)[(kg * kDqNTiles + nt) * 32 + lane] = make_uint2(b[0], b[1]);
+  }
+  // xs: thread (m, r) of the first 256 takes row r; a butterfly over the warp's
+  // 32 rows, then the two warps of each row of X in order
+  __shared__ float wsum[8];
+  {
+    __nv_bfloat16 hi, lo;
+    split_hi_lo(xprime(X, M, D_in, s, tid / kDqRows, ch * kDqRows + tid % kDqRows), hi, lo);
+    float v = __bfloat162float(hi) + __bfloat162float(lo);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) wsum[tid >> 5] = v;
+  }
+  __syncthreads();
+  if (tid < 4) reinterpret_cast<float*>(dst + kDqFragBytes)[tid] = wsum[2 * tid] + wsum[2 * tid + 1];
+}
+
+// The CTA whose run holds stage b: the largest c with floor(c B / ctas) <= b.
+__device__ __forceinline__ int64_t dq_cta_of(int64_t b, int64_t B, int64_t ctas) { return ((b + 1) * ctas - 1) / B; }
+
+template <int NT>
+__global__ void __launch_bounds__(kDqThreads, kDqCtasPerSm)
+    w4a16_decode_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSc,
+                        const __grid_constant__ CUtensorMap tmZ, const uint8_t* __restrict__ xf, int M,
+                        int64_t D_in, int64_t D_out, int group_size, uint32_t bias, float* __restrict__ partial,
+                        unsigned int* __restrict__ tickets, __nv_bfloat16* __restrict__ Y, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kDqStages];
+  __shared__ __align__(8) uint64_t empty_bar[kDqStages];
+  __shared__ int abort_sh;
+  __shared__ bool last;
+  volatile int* abort_flag = &abort_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nch = D_in / kDqRows;                       // 64-row chunks per column block
+  const int64_t ncb = (D_out + kDqCols - 1) / kDqCols;
+  const int64_t B = nch * ncb, ctas = gridDim.x;
+  const int64_t b_begin = static_cast<int64_t>(blockIdx.x) * B / ctas;
+  const int64_t b_end = (static_cast<int64_t>(blockIdx.x) + 1) * B / ctas;
+  const int64_t cpg = group_size / kDqRows;                 // chunks per group
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kDqStages; ++st) {
+      mbar_init(&full_bar[st], 1);
+      mbar_init(&empty_bar[st], kDqConsumers);
+    }
+    abort_sh = 0;
+    fence_mbar_init();
   }
   __syncthreads();
 
-  const int64_t n = n0 + lane * 8;
-  float acc[MT][8];  // sum_j x'_j q_j of the warp's rows, then its share of Y
+  if (warp == kDqConsumers) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmC);
+      prefetch_tmap(&tmSc);
+      prefetch_tmap(&tmZ);
+      auto issue_codes_sides = [&](int st, int64_t cb, int64_t ch) {
+        uint8_t* stage = smem + st * kDqStageStride;
+        mbar_arrive_expect_tx(&full_bar[st], kDqStageTx);
+        const int32_t c0 = static_cast<int32_t>(cb * kDqCols);
 #pragma unroll
-  for (int m = 0; m < MT; ++m)
+        for (int q = 0; q < kDqCols / kDqBoxCols; ++q)
+          tma_load_2d(stage + q * kDqBoxBytes, &tmC, &full_bar[st], c0 + q * kDqBoxCols,
+                      static_cast<int32_t>(ch * kDqByteRows));
+        const int32_t g = static_cast<int32_t>(ch / cpg);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc[m][c] = 0.f;
-  const int wr = warp * 32;  // the warp's first row within the CTA
-  if (wr < rows && n < D_out) {
-    const uint8_t* qb = qweight + ((r0 + wr) / 2) * D_out + n;
-    // the warp's 16 byte rows in batches whose loads are all in flight: one
-    // batch of 16 for one or two rows of X, two of 8 when the accumulators
-    // need the registers
-    constexpr int kBatch = MT <= 2 ? 16 : 8;
-#pragma unroll
-    for (int h = 0; h < 16 / kBatch; ++h) {
-      uint2 cb[kBatch];
-#pragma unroll
-      for (int p = 0; p < kBatch; ++p) cb[p] = *reinterpret_cast<const uint2*>(qb + (kBatch * h + p) * D_out);
-#pragma unroll
-      for (int p = 0; p < kBatch; ++p) {
-#pragma unroll
-        for (int odd = 0; odd < 2; ++odd) {
-          float t0[4], t1[4];
-          nibbles_to_f32(odd ? (cb[p].x >> 4) & 0x0F0F0F0Fu : cb[p].x & 0x0F0F0F0Fu, t0);
-          nibbles_to_f32(odd ? (cb[p].y >> 4) & 0x0F0F0F0Fu : cb[p].y & 0x0F0F0F0Fu, t1);
-          float qc[8];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            qc[k] = t0[k] - 8388608.0f;  // the code, exact
-            qc[4 + k] = t1[k] - 8388608.0f;
-          }
-#pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            const float x = xs[m][wr + 2 * (kBatch * h + p) + odd];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) acc[m][c] = fmaf(x, qc[c], acc[m][c]);
+        for (int q = 0; q < kDqCols / kDqSideBox; ++q) {
+          tma_load_2d(stage + kDqOffSc + q * kDqSideBox * 2, &tmSc, &full_bar[st], c0 + q * kDqSideBox, g);
+          tma_load_2d(stage + kDqOffZ + q * kDqSideBox * 2, &tmZ, &full_bar[st], c0 + q * kDqSideBox, g);
+        }
+      };
+      auto issue_frag = [&](int st, int64_t ch) {
+        bulk_g2s_dq(smem + st * kDqStageStride + kDqOffFrag, xf + ch * kDqChunkBytes, kDqChunkBytes, &full_bar[st]);
+      };
+      // The first stages' codes and scales do not depend on the x' preparation
+      // that may still run: issue them, then wait for it, then its fragments.
+      const int pre = static_cast<int>(b_end - b_begin < kDqStages ? b_end - b_begin : kDqStages);
+      {
+        int64_t cb = b_begin / nch, ch = b_begin % nch;
+        for (int j = 0; j < pre; ++j) {
+          issue_codes_sides(j, cb, ch);
+          if (++ch == nch) {
+            ch = 0;
+            ++cb;
           }
         }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        ch = b_begin % nch;
+        for (int j = 0; j < pre; ++j) {
+          issue_frag(j, ch);
+          if (++ch == nch) ch = 0;
+        }
       }
-    }
-    // the warp's rows lie in one group: scale and zero of its 8 columns
-    const int64_t g = (r0 + wr) / group_size;
-    const uint4 hs = *reinterpret_cast<const uint4*>(scales + g * D_out + n);
-    const uint4 hz = *reinterpret_cast<const uint4*>(zeros + g * D_out + n);
-    const uint32_t us[4] = {hs.x, hs.y, hs.z, hs.w};
-    const uint32_t uz[4] = {hz.x, hz.y, hz.z, hz.w};
-    float sc[8], zc[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&us[k]));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&uz[k]));
-      sc[2 * k] = a.x;
-      sc[2 * k + 1] = a.y;
-      zc[2 * k] = b.x;
-      zc[2 * k + 1] = b.y;
-    }
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      float xsum = 0.f;
-#pragma unroll 8
-      for (int r = 0; r < 32; ++r) xsum += xs[m][wr + r];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) acc[m][c] = sc[c] * fmaf(-zc[c], xsum, acc[m][c]);
-    }
-  }
-  // the 8 warps' shares in a fixed order: (w0 + w4) + (w1 + w5) + (w2 + w6) + (w3 + w7)
-  if (warp < 4) {
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      float4* dst = reinterpret_cast<float4*>(&red[warp][m][lane * 8]);
-      dst[0] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-      dst[1] = make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
-    }
-  }
-  __syncthreads();
-  if (warp >= 4) {
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      float4* dst = reinterpret_cast<float4*>(&red[warp - 4][m][lane * 8]);
-      const float4 a = dst[0], b = dst[1];
-      dst[0] = make_float4(a.x + acc[m][0], a.y + acc[m][1], a.z + acc[m][2], a.w + acc[m][3]);
-      dst[1] = make_float4(b.x + acc[m][4], b.y + acc[m][5], b.z + acc[m][6], b.w + acc[m][7]);
-    }
-  }
-  __syncthreads();
-  const int64_t rb_count = gridDim.y;
-  for (int i = t; i < MT * kDecCols; i += kDecThreads) {
-    const int m = i / kDecCols, c = i % kDecCols;
-    if (m < M && n0 + c < D_out) {
-      const float v = (red[0][m][c] + red[1][m][c]) + (red[2][m][c] + red[3][m][c]);
-      partial[(static_cast<int64_t>(blockIdx.y) * M + m) * D_out + n0 + c] = v;
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (t == 0) last = atomicAdd(&tickets[blockIdx.x], 1u) == static_cast<unsigned>(rb_count) - 1u;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  for (int i = t; i < MT * kDecCols; i += kDecThreads) {
-    const int m = i / kDecCols, c = i % kDecCols;
-    if (m < M && n0 + c < D_out) {
-      // 16 row blocks' loads in flight, each batch as a fixed pairwise fp32
-      // tree, the batches in order (fp64 adds are slow on this part)
-      float v = 0.f;
-      for (int64_t b0 = 0; b0 < rb_count; b0 += 16) {
-        float pv[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          pv[k] = b0 + k < rb_count ? partial[((b0 + k) * M + m) * D_out + n0 + c] : 0.f;
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int k = 0; k < w; ++k) pv[k] += pv[k + w];
-        v += pv[0];
+      int64_t cb = (b_begin + pre) / nch, ch = (b_begin + pre) % nch;
+      int it = pre;
+      bool ok = true;
+      for (int64_t b = b_begin + pre; b < b_end; ++b, ++it) {
+        const int st = it % kDqStages;
+        if (!mbar_wait(&empty_bar[st], ((it / kDqStages) + 1) & 1, status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        issue_codes_sides(st, cb, ch);
+        issue_frag(st, ch);
+        if (++ch == nch) {
+          ch = 0;
+          ++cb;
+        }
       }
-      Y[static_cast<int64_t>(m) * D_out + n0 + c] = __float2bfloat16_rn(v);
+      // after an abort, the copies still in flight land before the CTA exits
+      if (!ok || *abort_flag)
+        for (int j = it - kDqStages < 0 ? 0 : it - kDqStages; j < it; ++j)
+          mbar_wait(&full_bar[j % kDqStages], (j / kDqStages) & 1, nullptr, nullptr, kCopyDrainNs);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the tickets are zeroed by the preparation grid
+  const int g = lane >> 2, t = lane & 3;
+  // this lane's output: rows m = 2nt + (t & 1) of X, columns 8g + 4u + 2(t >> 1) + {0, 1} (u = 0, 1)
+  const int ccol = warp * kDqWarpCols + 8 * g + 2 * (t >> 1);
+  int64_t cb = b_begin / nch, ch = b_begin % nch;
+  int64_t gch = ch % cpg;  // chunk index within its group
+  int st = 0;
+  uint32_t phase = 0;
+  bool ok = true;    // false once a wait gave up; the warps leave together
+  float y[NT][4];    // [n tile][2u + column offset]
+  float d[NT][2][4];  // the group's MMA sums per n tile and MMA tile u
+  float xs[NT];      // the group's row sums of x'_hi + x'_lo, rows 2nt + (t & 1) of X
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    xs[n] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) y[n][j] = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) d[n][u][k] = 0.f;
+  }
+  // Shared-memory byte offsets within a stage.  The warp's 64 columns are half
+  // (warp & 1) of tensor copy warp / 2; the lane's 8 bytes of byte row p sit in
+  // the 16-byte unit ((warp & 1) * 4 + g / 2) ^ (p & 7).  A k group of parity par
+  // in block b of 8 byte rows takes byte row 8b + 2t + par, whose p & 7 = 2t + par.
+  const uint32_t unit = (warp & 1) * 4 + (g >> 1);
+  const uint32_t code_off = (warp >> 1) * kDqBoxBytes + (g & 1) * 8;
+  const uint32_t row_off0 = code_off + (2 * t) * 128 + ((unit ^ (2 * t)) << 4);
+  const uint32_t row_off1 = code_off + (2 * t + 1) * 128 + ((unit ^ (2 * t + 1)) << 4);
+  const uint32_t frag_off = kDqOffFrag + lane * 8;
+  const uint32_t smem_base = smem_u32(smem);
+  for (int64_t b = b_begin; b < b_end; ++b) {
+    if (ok && !mbar_wait(&full_bar[st], phase, status, abort_flag)) ok = false;
+    const bool seg_end = ch == nch - 1 || b == b_end - 1;
+    if (ok) {
+      const uint32_t sa = smem_base + st * kDqStageStride;
+#pragma unroll
+      for (int kg = 0; kg < kDqKGroups; ++kg) {
+        // byte row 8 (kg / 2) + 2t + (kg & 1): input rows 2p (low nibbles) and 2p + 1
+        const uint2 cwd = lds_u32x2(sa + ((kg & 1) ? row_off1 : row_off0) + (kg >> 1) * 1024);
+        const uint32_t w[2] = {cwd.x, cwd.y};
+        uint2 bf[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) bf[n] = lds_u32x2(sa + frag_off + (kg * kDqNTiles + n) * 256);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint32_t a0 = code_pair(w[u], bias), a1 = code_pair(w[u] >> 8, bias);
+          const uint32_t a2 = code_pair(w[u] >> 4, bias), a3 = code_pair(w[u] >> 12, bias);
+#pragma unroll
+          for (int n = 0; n < NT; ++n) mma_bf16_16816(d[n][u], a0, a1, a2, a3, bf[n].x, bf[n].y);
+        }
+      }
+      const uint8_t* stage = smem + st * kDqStageStride;
+      const float* xsum = reinterpret_cast<const float*>(stage + kDqOffFrag + kDqFragBytes);
+#pragma unroll
+      for (int n = 0; n < NT; ++n) xs[n] += xsum[2 * n + (t & 1)];
+      if (gch == cpg - 1 || seg_end) {
+        // the group (or the run's part of it) ends: y += sc (D_hi + D_lo - (z + 128) xs)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(stage + kDqOffSc + (ccol + 4 * u) * 2));
+          const float2 z = __half22float2(*reinterpret_cast<const __half2*>(stage + kDqOffZ + (ccol + 4 * u) * 2));
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            y[n][2 * u] = fmaf(sc.x, fmaf(-(z.x + 128.f), xs[n], d[n][u][0] + d[n][u][1]), y[n][2 * u]);
+            y[n][2 * u + 1] = fmaf(sc.y, fmaf(-(z.y + 128.f), xs[n], d[n][u][2] + d[n][u][3]), y[n][2 * u + 1]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) d[n][u][k] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n) xs[n] = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[st]);  // the warp is done with the stage
+    }
+    if (++st == kDqStages) {
+      st = 0;
+      phase ^= 1u;
+    }
+    if (++gch == cpg) gch = 0;
+    if (seg_end) {
+      if (named_bar_or(1, kDqConsumers * 32, !ok)) return;  // all consumer warps, after an abort
+      const int64_t slot = blockIdx.x + cb;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const int m = 2 * n + (t & 1);
+        if (m < M) {
+          float* dst = partial + (slot * M + m) * kDqCols + ccol;
+          *reinterpret_cast<float2*>(dst) = make_float2(y[n][0], y[n][1]);
+          *reinterpret_cast<float2*>(dst + 4) = make_float2(y[n][2], y[n][3]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) y[n][j] = 0.f;
+      }
+      __threadfence();
+      named_bar_sync(1, kDqConsumers * 32);
+      const int64_t c_first = dq_cta_of(cb * nch, B, ctas), c_last = dq_cta_of((cb + 1) * nch - 1, B, ctas);
+      if (threadIdx.x == 0) last = atomicAdd(&tickets[cb], 1u) == static_cast<unsigned>(c_last - c_first);
+      named_bar_sync(1, kDqConsumers * 32);
+      if (last) {
+        __threadfence();
+        const int64_t nseg = c_last - c_first + 1;
+        // thread k sums columns k and k + 512 of the block for every row of X
+        const int k0 = threadIdx.x;
+        for (int m = 0; m < M; ++m) {
+#pragma unroll 1
+          for (int q = 0; q < kDqCols / (kDqConsumers * 32); ++q) {
+            const int64_t col = cb * kDqCols + q * kDqConsumers * 32 + k0;
+            const float* src = partial + ((c_first + cb) * M + m) * kDqCols + q * kDqConsumers * 32 + k0;
+            float v = 0.f;
+            for (int64_t b0 = 0; b0 < nseg; b0 += 8) {
+              // the segments in batches of 8, each a fixed pairwise fp32 tree, the batches in order
+              float pv[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) pv[k] = b0 + k < nseg ? __ldcg(src + (b0 + k) * M * kDqCols) : 0.f;
+#pragma unroll
+              for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int k = 0; k < w; ++k) pv[k] += pv[k + w];
+              v += pv[0];
+            }
+            if (col < D_out) Y[static_cast<int64_t>(m) * D_out + col] = __float2bfloat16_rn(v);
+          }
+        }
+        if (threadIdx.x == 0) tickets[cb] = 0u;  // ready for the next call
+      }
+      named_bar_sync(1, kDqConsumers * 32);  // `last` is rewritten at the next segment's end
+    }
+    if (++ch == nch) {
+      ch = 0;
+      gch = 0;
+      ++cb;
     }
   }
-  if (t == 0) tickets[blockIdx.x] = 0u;  // ready for the next call
 }
 
 }  // namespace
 
 int64_t w4a16_decode_partial_floats(int64_t M, int64_t D_in, int64_t D_out) {
-  return ((D_in + kDecRows - 1) / kDecRows) * M * D_out;
+  (void)D_in;
+  return (kDqMaxCtas + (D_out + kDqCols - 1) / kDqCols) * M * kDqCols;
 }
-int64_t w4a16_decode_tickets(int64_t D_out) { return (D_out + kDecCols - 1) / kDecCols; }
+int64_t w4a16_decode_tickets(int64_t D_out) { return (D_out + kDqCols - 1) / kDqCols; }
+int64_t w4a16_decode_xprep_bytes(int64_t D_in) { return (D_in / kDqRows) * kDqChunkBytes; }
 
-cudaError_t launch_w4a16_decode(const void* X, int64_t M, int64_t D_in, int64_t D_out, const uint8_t* qweight,
-                                const void* scales, const void* zeros, const float* s, int group_size, void* Y,
-                                float* partial, unsigned int* tickets, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>((D_out + kDecCols - 1) / kDecCols),
-                  static_cast<unsigned>((D_in + kDecRows - 1) / kDecRows));
-  const auto* Xb = static_cast<const __nv_bfloat16*>(X);
-  const auto* sc = static_cast<const __half*>(scales);
-  const auto* zr = static_cast<const __half*>(zeros);
-  auto* Yb = static_cast<__nv_bfloat16*>(Y);
-  const int m = static_cast<int>(M);
-  if (M <= 1)
-    w4a16_decode_kernel<1><<<grid, kDecThreads, 0, stream>>>(Xb, m, D_in, D_out, qweight, sc, zr, s, group_size,
-                                                             partial, tickets, Yb);
-  else if (M <= 2)
-    w4a16_decode_kernel<2><<<grid, kDecThreads, 0, stream>>>(Xb, m, D_in, D_out, qweight, sc, zr, s, group_size,
-                                                             partial, tickets, Yb);
-  else
-    w4a16_decode_kernel<4><<<grid, kDecThreads, 0, stream>>>(Xb, m, D_in, D_out, qweight, sc, zr, s, group_size,
-                                                             partial, tickets, Yb);
+cudaError_t launch_w4a16_decode(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* X, int64_t M, int64_t D_in,
+                                int64_t D_out, const uint8_t* qweight, const void* scales, const void* zeros,
+                                const float* s, int group_size, void* Y, float* partial, unsigned int* tickets,
+                                uint8_t* xf, uint32_t* status, cudaStream_t stream) {
+  if (M < 1 || M > kW4a16DecodeMaxRows || D_in % kDqRows != 0 || group_size % kDqRows != 0)
+    return cudaErrorInvalidValue;
+  CUtensorMap tmC, tmSc, tmZ;
+  const cuuint32_t estr[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D_out), static_cast<cuuint64_t>(D_in / 2)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D_out)};
+    const cuuint32_t box[2] = {kDqBoxCols, kDqByteRows};
+    if (encode(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(qweight), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D_out), static_cast<cuuint64_t>(D_in / group_size)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D_out) * 2};
+    const cuuint32_t box[2] = {kDqSideBox, 1};
+    if (encode(&tmSc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(scales), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        encode(&tmZ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(zeros), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  // the CTAs that fit on the device, queried once per device (both kernels have the same footprint)
+  static std::atomic<int> resident[64];
+  auto kern = M <= 2 ? w4a16_decode_kernel<1> : w4a16_decode_kernel<2>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int fit = resident[dev].load(std::memory_order_acquire);
+  if (fit == 0) {
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDqThreads, kDqSmem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    fit = sms * per_sm;
+    resident[dev].store(fit, std::memory_order_release);
+  }
+  const int64_t nch = D_in / kDqRows;
+  const int64_t ncb = (D_out + kDqCols - 1) / kDqCols;
+  xprep_kernel<<<static_cast<unsigned>(nch), kXprepThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(X), static_cast<int>(M), D_in, s, xf, status, tickets, ncb);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the product starts while the preparation runs (its codes do not depend on it)
+  const int64_t ctas = std::min<int64_t>(std::min<int64_t>(fit, kDqMaxCtas), nch * ncb);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(kDqThreads);
+  cfg.dynamicSmemBytes = kDqSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, tmC, tmSc, tmZ, static_cast<const uint8_t*>(xf), static_cast<int>(M), D_in,
+                         D_out, group_size, kDqBias, partial, tickets, static_cast<__nv_bfloat16*>(Y), status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
