@@ -171,23 +171,54 @@ constexpr int kGpCols = kGpThreads;
 constexpr int kMaxGpCandidates = 21;  // candidates per CTA, the default grid (grid.z splits larger grids)
 constexpr int kGpChunk = 64;          // rows of W staged per step (16 KB)
 
+// The running range of one 64-row chunk for column t: for each quad of rows
+// the thread unpacks its four weights once, then per candidate takes the
+// quad's scales in one 16-byte broadcast load, forms w' = w s in two packed
+// multiplies and folds them into the range with two three-input min / max
+// operations.  FULL: all kMaxGpCandidates candidates are live (no per-candidate
+// test in the loop).
+template <bool FULL, bool SYM>
+__device__ __forceinline__ void range_chunk(const __nv_bfloat16* wsh, const float4* ssh, int t, int nk,
+                                            float (&lo)[kMaxGpCandidates], float (&hi)[kMaxGpCandidates]) {
+  const uint16_t* wcol = reinterpret_cast<const uint16_t*>(wsh) + t;
+#pragma unroll 1
+  for (int rq = 0; rq < kGpChunk / 4; ++rq) {
+    float w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = __uint_as_float(static_cast<uint32_t>(wcol[(4 * rq + i) * kGpCols]) << 16);
+    const float2 w01 = make_float2(w[0], w[1]), w23 = make_float2(w[2], w[3]);
+    const float4* sp = ssh + rq * (FULL ? kMaxGpCandidates : nk);
+#pragma unroll
+    for (int k = 0; k < kMaxGpCandidates; ++k) {
+      if (FULL || k < nk) {
+        const float4 sq = sp[k];
+        const float2 p = __fmul2_rn(w01, make_float2(sq.x, sq.y));
+        const float2 q = __fmul2_rn(w23, make_float2(sq.z, sq.w));
+        if (SYM) {
+          hi[k] = fmaxabs3(fmaxabs3(hi[k], p.x, p.y), q.x, q.y);
+        } else {
+          lo[k] = fmin3(fmin3(lo[k], p.x, p.y), q.x, q.y);
+          hi[k] = fmax3(fmax3(hi[k], p.x, p.y), q.x, q.y);
+        }
+      }
+    }
+  }
+}
+
 // One CTA: one group of GS rows x 128 columns, up to 21 candidates.  The group
 // streams through shared memory in 64-row chunks (W chunk 16 KB, the chunk's
-// scale rows as {s_k[r], s_k[r+1]} pairs so that one 8-byte broadcast load
-// feeds a packed multiply).  Thread t owns column t and keeps the running
-// range of all candidates in registers: for each pair of rows it unpacks its
-// two weights once, then per candidate does w' = w s for both rows in one
-// packed multiply and a three-input min / max against the running range.
+// scale rows as {s_k[r], .., s_k[r+3]} quads).  Thread t owns column t and
+// keeps the running range of all candidates in registers (range_chunk).
 // 22 KB of shared memory and <= 72 registers put 7 CTAs on an SM, so a
 // 4096 x 4096 layer's 1024 CTAs run in one wave.
 template <int GS>
-__global__ void __launch_bounds__(kGpThreads, 7) group_params_kernel(const __nv_bfloat16* __restrict__ W,
+__global__ void __launch_bounds__(kGpThreads, 6) group_params_kernel(const __nv_bfloat16* __restrict__ W,
                                                                 const float* __restrict__ s_tab, int64_t D_in,
                                                                 int64_t D_out, int G, int symmetric,
                                                                 float* __restrict__ qp, uint32_t* status) {
   extern __shared__ __align__(16) uint8_t smem[];
   __nv_bfloat16* wsh = reinterpret_cast<__nv_bfloat16*>(smem);            // [64][128]
-  float2* ssh = reinterpret_cast<float2*>(smem + kGpChunk * kGpCols * 2);  // [32][nk]
+  float4* ssh = reinterpret_cast<float4*>(smem + kGpChunk * kGpCols * 2);  // [16][nk]
   const int t = threadIdx.x;
   const int k0 = blockIdx.z * kMaxGpCandidates;
   const int nk = min(kMaxGpCandidates, G - k0);
@@ -226,52 +257,38 @@ __global__ void __launch_bounds__(kGpThreads, 7) group_params_kernel(const __nv_
       }
     }
     {
-      // scale pairs of the chunk, up to kMaxGpCandidates * 32 of them (rounded
+      // scale quads of the chunk, up to kMaxGpCandidates * 16 of them (rounded
       // up to whole rounds of the CTA; the k < nk test skips the overhang)
-      constexpr int kSLoads = (kMaxGpCandidates * (kGpChunk / 2) + kGpThreads - 1) / kGpThreads;
-      float2 sv[kSLoads];
+      constexpr int kSLoads = (kMaxGpCandidates * (kGpChunk / 4) + kGpThreads - 1) / kGpThreads;
+      float4 sv[kSLoads];
 #pragma unroll
       for (int i = 0; i < kSLoads; ++i) {
         const int idx = t + i * kGpThreads;
-        const int k = idx / (kGpChunk / 2);
-        const int rp = idx - k * (kGpChunk / 2);
-        sv[i] = k < nk ? *reinterpret_cast<const float2*>(s_tab + static_cast<int64_t>(k0 + k) * D_in + j0 + 2 * rp)
-                       : make_float2(0.f, 0.f);
+        const int k = idx / (kGpChunk / 4);
+        const int rq = idx - k * (kGpChunk / 4);
+        sv[i] = k < nk ? *reinterpret_cast<const float4*>(s_tab + static_cast<int64_t>(k0 + k) * D_in + j0 + 4 * rq)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int i = 0; i < kSLoads; ++i) {
         const int idx = t + i * kGpThreads;
-        const int k = idx / (kGpChunk / 2);
-        const int rp = idx - k * (kGpChunk / 2);
-        if (k < nk) ssh[rp * nk + k] = sv[i];
+        const int k = idx / (kGpChunk / 4);
+        const int rq = idx - k * (kGpChunk / 4);
+        if (k < nk) ssh[rq * nk + k] = sv[i];
       }
     }
     __syncthreads();
     if (n < D_out) {
-      const uint16_t* wcol = reinterpret_cast<const uint16_t*>(wsh) + t;
-#pragma unroll 2
-      for (int rp = 0; rp < kGpChunk / 2; ++rp) {
-        const float2 w2 = make_float2(__uint_as_float(static_cast<uint32_t>(wcol[(2 * rp) * kGpCols]) << 16),
-                                      __uint_as_float(static_cast<uint32_t>(wcol[(2 * rp + 1) * kGpCols]) << 16));
-        const float2* sp = ssh + rp * nk;
-        if (symmetric) {
-#pragma unroll
-          for (int k = 0; k < kMaxGpCandidates; ++k) {
-            if (k < nk) {
-              const float2 p = __fmul2_rn(w2, sp[k]);
-              hi[k] = fmaxabs3(hi[k], p.x, p.y);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < kMaxGpCandidates; ++k) {
-            if (k < nk) {
-              const float2 p = __fmul2_rn(w2, sp[k]);
-              lo[k] = fmin3(lo[k], p.x, p.y);
-              hi[k] = fmax3(hi[k], p.x, p.y);
-            }
-          }
-        }
+      if (nk == kMaxGpCandidates) {
+        if (symmetric)
+          range_chunk<true, true>(wsh, ssh, t, nk, lo, hi);
+        else
+          range_chunk<true, false>(wsh, ssh, t, nk, lo, hi);
+      } else {
+        if (symmetric)
+          range_chunk<false, true>(wsh, ssh, t, nk, lo, hi);
+        else
+          range_chunk<false, false>(wsh, ssh, t, nk, lo, hi);
       }
     }
   }
@@ -311,7 +328,7 @@ __global__ void __launch_bounds__(kGpThreads, 7) group_params_kernel(const __nv_
 }
 
 static size_t group_params_smem(int) {
-  return static_cast<size_t>(kGpChunk) * kGpCols * 2 + static_cast<size_t>(kGpChunk / 2) * kMaxGpCandidates * 8;
+  return static_cast<size_t>(kGpChunk) * kGpCols * 2 + static_cast<size_t>(kGpChunk / 4) * kMaxGpCandidates * 16;
 }
 
 template <int GS>
