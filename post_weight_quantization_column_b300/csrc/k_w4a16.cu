@@ -574,6 +574,8 @@ constexpr int64_t kDqMaxCtas = 1024;                       // bound of the grid 
 constexpr uint32_t kDqBias = 0x43004300u;                  // bf16 pair (128, 128)
 static_assert(kDqSmem <= 227 * 1024 && kDqCtasPerSm * (kDqSmem + 1024) <= 228 * 1024, "shared memory per SM");
 static_assert(kDqChunkBytes % 16 == 0 && kDqOffSc % 128 == 0 && kDqOffZ % 128 == 0, "copy alignment");
+static_assert(kDqOffFrag + kDqChunkBytes <= kDqOffSc && kDqOffZ + kDqSideBytes <= kDqStageStride,
+              "every region a stage is read at lies inside the stage");
 
 __device__ __forceinline__ void bulk_g2s_dq(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
   asm volatile(
