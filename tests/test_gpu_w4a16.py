@@ -70,10 +70,15 @@ def _layer(seed, M, D_in, D_out, g, sym, alpha=0.5, w_sigma=0.02):
 CASES = [
     # M, D_in, D_out, group, symmetric: ragged rows (not a multiple of 512), ragged
     # columns (not a multiple of 256), several K steps per group, every group size;
-    # M <= 4 takes the decode path (row blocks of 256 with a ragged last block)
+    # M <= 4 takes the decode path: 64-row x 1024-column stages in contiguous runs per
+    # CTA -- one stage per CTA, runs that cross column blocks, column blocks whose
+    # segments need more than one batch of the final sum, a ragged last block
     (1, 256, 272, 128, False),
     (2, 320, 784, 64, True),
     (3, 768, 1040, 256, False),
+    (1, 64, 8192, 64, True),
+    (4, 1024, 28672, 128, False),
+    (2, 8192, 2048, 256, True),
     (5, 1024, 528, 128, True),
     (8, 576, 4096, 64, False),
     (200, 384, 784, 64, True),
