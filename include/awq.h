@@ -382,10 +382,15 @@ AWQ_API awq_status awq_greedy_search(const void* W, const float* mean_abs, int64
  *   ws       device workspace of awq_w4a16_workspace_size(M, D_in, D_out) bytes
  * M > 4 (prefill): each weight enters the tensor cores as bf16(((code -
  * zero) * scale) * RN(1/s_j)) and the products accumulate in fp32.  M <= 4
- * (decode): CUDA cores read each code once and form, per group, scale *
- * (sum_j x'_j code_j - zero * sum_j x'_j) with x' = fp32(x / s) and fp32
- * sums, the row blocks added in a fixed order in fp64.  Y is rounded to
- * bf16.  Shapes: D_in a multiple of 64 and of group_size, D_out a multiple
+ * (decode): each code is read once and enters the tensor cores as the exact
+ * bf16 value 128 + code, against x' = fp32(x / s) split into bf16 hi + lo
+ * parts; per group the kernel forms scale * (D - (zero + 128) * sum_j x'_j)
+ * with fp32 sums, and adds the per-CTA segments in a fixed order (fp32
+ * trees of 8).  Y is rounded to bf16.  The decode form writes the workspace
+ * header and its ticket counters itself (its first kernel zeroes them), and
+ * its product kernel may begin before that kernel ends (programmatic
+ * dependent launch; nothing it reads from the first kernel is read before
+ * it waits for it).  Shapes: D_in a multiple of 64 and of group_size, D_out a multiple
  * of 16; all pointers 16-byte aligned (ws 256).  M = 0 is a no-op.  A
  * timeout of the kernel's bounded waits sets AWQ_ERR_TIMEOUT in the status
  * word.
