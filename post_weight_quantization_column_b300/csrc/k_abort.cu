@@ -34,14 +34,6 @@ constexpr int kAbortThreads = 256;
 constexpr int kAbortCopyBytes = 4096;
 constexpr uint32_t kAbortTmemCols = 32;
 
-__device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // record[0]: CTAs that reached the end and freed TMEM; record[1]: CTAs in
 // which a wait expired (the abort flag is raised only then); record[2]: the
 // largest time (us) a CTA spent from its start to its end; record[3]: CTAs

@@ -577,14 +577,6 @@ static_assert(kDqChunkBytes % 16 == 0 && kDqOffSc % 128 == 0 && kDqOffZ % 128 ==
 static_assert(kDqOffFrag + kDqChunkBytes <= kDqOffSc && kDqOffZ + kDqSideBytes <= kDqStageStride,
               "every region a stage is read at lies inside the stage");
 
-__device__ __forceinline__ void bulk_g2s_dq(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // (x & 0x000F000F) | bias in one logic operation (bias kept in a register).
 __device__ __forceinline__ uint32_t code_pair(uint32_t x, uint32_t bias) {
   uint32_t d;
@@ -727,7 +719,7 @@ __global__ void __launch_bounds__(kDqThreads, kDqCtasPerSm)
         }
       };
       auto issue_frag = [&](int st, int64_t ch) {
-        bulk_g2s_dq(smem + st * kDqStageStride + kDqOffFrag, xf + ch * kDqChunkBytes, kDqChunkBytes, &full_bar[st]);
+        bulk_copy_g2s(smem + st * kDqStageStride + kDqOffFrag, xf + ch * kDqChunkBytes, kDqChunkBytes, &full_bar[st]);
       };
       // The first stages' codes and scales do not depend on the x' preparation
       // that may still run: issue them, then wait for it, then its fragments.
