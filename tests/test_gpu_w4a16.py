@@ -11,6 +11,11 @@ times |Y|), so the relative Frobenius error is also held to 2^-7, about five
 times the expected size of the rounding noise: a systematic slip (a wrong
 group's scale, a dropped zero) moves it by far more.
 
+The decode form (M <= 4) stays well inside the same bound: its codes enter
+the tensor cores as the exact bf16 values 128 + code, against x' = x / s split
+into bf16 hi + lo parts (2^-16 of x'); the products are exact, the sums fp32,
+and the 128 bias comes off with the group's fp32 row sum before the scale.
+
 The oracle's packed inputs always come from the oracle's own pack; the GPU
 runs on the GPU pack, which these tests first check to be bit-identical.
 """
